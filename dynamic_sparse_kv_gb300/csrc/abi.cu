@@ -1,0 +1,339 @@
+// C ABI of libfastocr.so (declared in include/fastocr.h): argument checking,
+// the workspace, split-K sizing and kernel dispatch. Host code only.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "attend_kernels.cuh"
+#include "fastocr.h"
+
+namespace fastocr {
+cudaError_t launch_bf16(int head_dim, int mode, const Params& p, cudaStream_t s);
+cudaError_t launch_f32(int head_dim, int mode, const Params& p, cudaStream_t s);
+cudaError_t prepare_bf16();
+cudaError_t prepare_f32();
+}  // namespace fastocr
+
+using namespace fastocr;
+
+struct fastocr_handle {
+  fastocr_dims dims;
+  int device;
+  int num_sms;
+  int log2_page;
+  int split_override[3];
+  void* ws;
+  size_t ws_bytes;
+  float* part_ml;
+  float* part_acc;
+  float* logits;
+  float* sigma_part;
+  int32_t* cnt_head;
+  int32_t* cnt_seq;
+  double* profile;
+  int32_t* status;
+};
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int ilog2_exact(int x) {
+  int l = 0;
+  while ((1 << l) < x) ++l;
+  return (1 << l) == x ? l : -1;
+}
+
+// Split-K factor: minimise (waves of CTAs) / splits + a small per-split merge
+// cost, with 2 resident CTAs per SM, at most one 64-token tile per split.
+int auto_splits(const fastocr_handle* h) {
+  const long units = (long)h->dims.batch * h->dims.num_kv_heads;
+  const long slots = (long)h->num_sms * 2;
+  const long max_tokens = (long)h->dims.max_pages_per_seq << h->log2_page;
+  const int max_useful = (int)std::max(1L, std::min<long>(kMaxSplits, (max_tokens + 63) / 64));
+  int best = 1;
+  double best_cost = 1e300;
+  for (int s = 1; s <= max_useful; ++s) {
+    const long waves = (units * s + slots - 1) / slots;
+    const double cost = (double)waves / s + 0.004 * s;
+    if (cost < best_cost - 1e-12) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+int splits_for(const fastocr_handle* h, int mode_slot) {
+  const int o = h->split_override[mode_slot];
+  return o > 0 ? o : auto_splits(h);
+}
+
+fastocr_status check_kv(const fastocr_handle* h, const fastocr_kv* kv) {
+  if (!kv || !kv->k || !kv->v || !kv->block_table || !kv->seq_len) return FASTOCR_ERR_NULL;
+  if (kv->num_pages < 1) return FASTOCR_ERR_INVALID;
+  if (!aligned16(kv->k) || !aligned16(kv->v)) return FASTOCR_ERR_ALIGN;
+  (void)h;
+  return FASTOCR_OK;
+}
+
+Params base_params(const fastocr_handle* h, const void* q, const fastocr_kv* kv, void* out) {
+  Params p;
+  memset(&p, 0, sizeof(p));
+  const fastocr_dims& d = h->dims;
+  p.q = q;
+  p.out = out;
+  p.k = kv->k;
+  p.v = kv->v;
+  p.block_table = kv->block_table;
+  p.seq_len = kv->seq_len;
+  p.num_pages = kv->num_pages;
+  p.max_pages = d.max_pages_per_seq;
+  p.log2_page = h->log2_page;
+  p.B = d.batch;
+  p.Hq = d.num_q_heads;
+  p.Hkv = d.num_kv_heads;
+  p.g = d.num_q_heads / d.num_kv_heads;
+  p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d.head_dim));
+  p.part_ml = h->part_ml;
+  p.part_acc = h->part_acc;
+  p.logits = h->logits;
+  p.sigma_part = h->sigma_part;
+  p.cnt_head = h->cnt_head;
+  p.cnt_seq = h->cnt_seq;
+  p.profile = h->profile;
+  p.profile_layer = -1;
+  p.status = h->status;
+  p.max_img = d.max_img_tokens;
+  return p;
+}
+
+fastocr_status launch(const fastocr_handle* h, int mode, const Params& p, fastocr_stream stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = h->dims.dtype == FASTOCR_DTYPE_BF16 ? launch_bf16(h->dims.head_dim, mode, p, s)
+                                                       : launch_f32(h->dims.head_dim, mode, p, s);
+  return e == cudaSuccess ? FASTOCR_OK : FASTOCR_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t fastocr_abi_version(void) { return FASTOCR_ABI_VERSION; }
+
+const char* fastocr_status_string(int32_t status) {
+  switch (status) {
+    case FASTOCR_OK: return "ok";
+    case FASTOCR_ERR_NULL: return "a required pointer is NULL";
+    case FASTOCR_ERR_INVALID: return "an argument is out of range";
+    case FASTOCR_ERR_UNSUPPORTED: return "shape not supported by the kernels";
+    case FASTOCR_ERR_CUDA: return "a CUDA runtime call failed";
+    case FASTOCR_ERR_NO_DEVICE: return "no usable sm_103 CUDA device";
+    case FASTOCR_ERR_ALIGN: return "a device pointer is not 16-byte aligned";
+  }
+  return "unknown status";
+}
+
+fastocr_status fastocr_create(const fastocr_dims* dims, fastocr_handle** out) {
+  if (!dims || !out) return FASTOCR_ERR_NULL;
+  const fastocr_dims d = *dims;
+  if (d.batch < 1 || d.num_q_heads < 1 || d.num_kv_heads < 1 || d.max_pages_per_seq < 1 ||
+      d.num_layers < 1 || d.max_img_tokens < 0 || d.page_size < 1 || d.page_size > 256)
+    return FASTOCR_ERR_INVALID;
+  if (d.num_q_heads % d.num_kv_heads != 0) return FASTOCR_ERR_INVALID;
+  if (d.dtype != FASTOCR_DTYPE_F32 && d.dtype != FASTOCR_DTYPE_BF16) return FASTOCR_ERR_INVALID;
+  const int log2_page = ilog2_exact(d.page_size);
+  if (log2_page < 0) return FASTOCR_ERR_INVALID;
+  if (d.num_q_heads / d.num_kv_heads > kSlots) return FASTOCR_ERR_UNSUPPORTED;
+  if (d.head_dim != 64 && d.head_dim != 128) return FASTOCR_ERR_UNSUPPORTED;
+  if (d.max_img_tokens > kMaxImg) return FASTOCR_ERR_UNSUPPORTED;
+  if ((long long)d.max_pages_per_seq * d.page_size >= (1LL << 30)) return FASTOCR_ERR_UNSUPPORTED;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FASTOCR_ERR_NO_DEVICE;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FASTOCR_ERR_NO_DEVICE;
+  if (prop.major != 10 || prop.minor != 3) return FASTOCR_ERR_NO_DEVICE;
+  if (prepare_bf16() != cudaSuccess || prepare_f32() != cudaSuccess) return FASTOCR_ERR_CUDA;
+
+  const size_t units = (size_t)d.batch * d.num_kv_heads;
+  const size_t img = (size_t)d.max_img_tokens;
+  size_t off = 0;
+  const size_t o_ml = off;
+  off = align_up(off + units * kMaxSplits * kSlots * 2 * sizeof(float), 256);
+  const size_t o_acc = off;
+  off = align_up(off + units * kMaxSplits * kSlots * d.head_dim * sizeof(float), 256);
+  const size_t o_logits = off;
+  off = align_up(off + units * img * kSlots * sizeof(float), 256);
+  const size_t o_sigma = off;
+  off = align_up(off + units * img * sizeof(float), 256);
+  const size_t o_zero = off;  // counters, profiler, status: zeroed once here
+  const size_t o_cnt_head = off;
+  off = align_up(off + units * sizeof(int32_t), 256);
+  const size_t o_cnt_seq = off;
+  off = align_up(off + (size_t)d.batch * sizeof(int32_t), 256);
+  const size_t o_profile = off;
+  off = align_up(off + (size_t)d.num_layers * sizeof(double), 256);
+  const size_t o_status = off;
+  off = align_up(off + sizeof(int32_t), 256);
+
+  fastocr_handle* h = static_cast<fastocr_handle*>(calloc(1, sizeof(fastocr_handle)));
+  if (!h) return FASTOCR_ERR_CUDA;
+  h->dims = d;
+  h->device = dev;
+  h->num_sms = prop.multiProcessorCount;
+  h->log2_page = log2_page;
+  h->ws_bytes = off;
+  if (cudaMalloc(&h->ws, off) != cudaSuccess) {
+    free(h);
+    return FASTOCR_ERR_CUDA;
+  }
+  char* base = static_cast<char*>(h->ws);
+  h->part_ml = reinterpret_cast<float*>(base + o_ml);
+  h->part_acc = reinterpret_cast<float*>(base + o_acc);
+  h->logits = reinterpret_cast<float*>(base + o_logits);
+  h->sigma_part = reinterpret_cast<float*>(base + o_sigma);
+  h->cnt_head = reinterpret_cast<int32_t*>(base + o_cnt_head);
+  h->cnt_seq = reinterpret_cast<int32_t*>(base + o_cnt_seq);
+  h->profile = reinterpret_cast<double*>(base + o_profile);
+  h->status = reinterpret_cast<int32_t*>(base + o_status);
+  if (cudaMemset(base + o_zero, 0, off - o_zero) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    cudaFree(h->ws);
+    free(h);
+    return FASTOCR_ERR_CUDA;
+  }
+  *out = h;
+  return FASTOCR_OK;
+}
+
+fastocr_status fastocr_destroy(fastocr_handle* h) {
+  if (!h) return FASTOCR_OK;
+  cudaError_t e = cudaDeviceSynchronize();
+  cudaError_t f = cudaFree(h->ws);
+  free(h);
+  return (e == cudaSuccess && f == cudaSuccess) ? FASTOCR_OK : FASTOCR_ERR_CUDA;
+}
+
+fastocr_status fastocr_full_attend(fastocr_handle* h, const void* q, const fastocr_kv* kv,
+                                   void* out, fastocr_stream stream) {
+  if (!h || !q || !out) return FASTOCR_ERR_NULL;
+  fastocr_status st = check_kv(h, kv);
+  if (st != FASTOCR_OK) return st;
+  if (!aligned16(q) || !aligned16(out)) return FASTOCR_ERR_ALIGN;
+  Params p = base_params(h, q, kv, out);
+  p.splits = splits_for(h, 0);
+  return launch(h, kFull, p, stream);
+}
+
+fastocr_status fastocr_focal_attend(fastocr_handle* h, const void* q, const fastocr_kv* kv,
+                                    const int32_t* img_range, double tau, void* out,
+                                    int32_t* idx, int32_t idx_stride, int32_t* k_out,
+                                    int32_t profile_layer, fastocr_stream stream) {
+  if (!h || !q || !out || !img_range || !idx || !k_out) return FASTOCR_ERR_NULL;
+  fastocr_status st = check_kv(h, kv);
+  if (st != FASTOCR_OK) return st;
+  if (!aligned16(q) || !aligned16(out)) return FASTOCR_ERR_ALIGN;
+  if (!(tau > 0.0 && tau <= 1.0)) return FASTOCR_ERR_INVALID;
+  if (h->dims.max_img_tokens < 1) return FASTOCR_ERR_INVALID;
+  if (idx_stride < keep_count(tau, h->dims.max_img_tokens)) return FASTOCR_ERR_INVALID;
+  if (profile_layer < -1 || profile_layer >= h->dims.num_layers) return FASTOCR_ERR_INVALID;
+  Params p = base_params(h, q, kv, out);
+  p.img_range = img_range;
+  p.tau = tau;
+  p.idx_out = idx;
+  p.idx_stride = idx_stride;
+  p.k_out = k_out;
+  p.profile_layer = profile_layer;
+  p.splits = splits_for(h, 0);
+  return launch(h, kFocal, p, stream);
+}
+
+fastocr_status fastocr_sparse_attend(fastocr_handle* h, const void* q, const fastocr_kv* kv,
+                                     const int32_t* img_range, const int32_t* idx,
+                                     int32_t idx_stride, const int32_t* k, void* out,
+                                     fastocr_stream stream) {
+  if (!h || !q || !out || !img_range || !idx || !k) return FASTOCR_ERR_NULL;
+  fastocr_status st = check_kv(h, kv);
+  if (st != FASTOCR_OK) return st;
+  if (!aligned16(q) || !aligned16(out)) return FASTOCR_ERR_ALIGN;
+  if (idx_stride < 1) return FASTOCR_ERR_INVALID;
+  Params p = base_params(h, q, kv, out);
+  p.img_range = img_range;
+  p.idx = idx;
+  p.idx_stride = idx_stride;
+  p.k_in = k;
+  p.splits = splits_for(h, 1);
+  return launch(h, kSparse, p, stream);
+}
+
+fastocr_status fastocr_rswa_attend(fastocr_handle* h, const void* q, const fastocr_kv* kv,
+                                   int32_t prefix_len, int32_t window, void* out,
+                                   fastocr_stream stream) {
+  if (!h || !q || !out) return FASTOCR_ERR_NULL;
+  fastocr_status st = check_kv(h, kv);
+  if (st != FASTOCR_OK) return st;
+  if (!aligned16(q) || !aligned16(out)) return FASTOCR_ERR_ALIGN;
+  if (prefix_len < 0 || window < 0) return FASTOCR_ERR_INVALID;
+  Params p = base_params(h, q, kv, out);
+  p.prefix_len = prefix_len;
+  p.window = window;
+  p.splits = splits_for(h, 2);
+  return launch(h, kRswa, p, stream);
+}
+
+fastocr_status fastocr_profiler_reset(fastocr_handle* h, fastocr_stream stream) {
+  if (!h) return FASTOCR_ERR_NULL;
+  cudaError_t e = cudaMemsetAsync(h->profile, 0, (size_t)h->dims.num_layers * sizeof(double),
+                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FASTOCR_OK : FASTOCR_ERR_CUDA;
+}
+
+fastocr_status fastocr_profiler_select(fastocr_handle* h, int32_t n_focal, int32_t* layers_out,
+                                       double* ratio_out, fastocr_stream stream) {
+  if (!h || !layers_out) return FASTOCR_ERR_NULL;
+  const int L = h->dims.num_layers;
+  if (n_focal < 1 || n_focal > L) return FASTOCR_ERR_INVALID;
+  std::vector<double> mass(L);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(mass.data(), h->profile, L * sizeof(double), cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return FASTOCR_ERR_CUDA;
+  std::vector<int> order(L);
+  for (int l = 0; l < L; ++l) order[l] = l;
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int a, int b) { return mass[a] > mass[b]; });  // ties keep lower id first
+  std::vector<int> chosen(order.begin(), order.begin() + n_focal);
+  std::sort(chosen.begin(), chosen.end());
+  for (int i = 0; i < n_focal; ++i) layers_out[i] = chosen[i];
+  if (ratio_out)
+    for (int l = 0; l < L; ++l) ratio_out[l] = mass[l];
+  return FASTOCR_OK;
+}
+
+fastocr_status fastocr_device_status(fastocr_handle* h, int32_t* status, fastocr_stream stream) {
+  if (!h || !status) return FASTOCR_ERR_NULL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, h->status, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess ||
+      cudaMemsetAsync(h->status, 0, sizeof(int32_t), s) != cudaSuccess)
+    return FASTOCR_ERR_CUDA;
+  *status = v;
+  return FASTOCR_OK;
+}
+
+fastocr_status fastocr_set_splits(fastocr_handle* h, int32_t mode, int32_t splits) {
+  if (!h) return FASTOCR_ERR_NULL;
+  if (mode < 0 || mode > 2 || splits < 0) return FASTOCR_ERR_INVALID;
+  h->split_override[mode] = splits == 0 ? 0 : std::min(std::max(splits, 1), kMaxSplits);
+  return FASTOCR_OK;
+}
+
+}  // extern "C"

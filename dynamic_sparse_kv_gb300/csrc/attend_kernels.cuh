@@ -1,0 +1,333 @@
+// Decode-attention kernels of FastOCR (focal / sparse) and R-SWA for sm_103a.
+//
+// One kernel template covers every layer kind; they differ only in the
+// attend list -- the ordered list of cache positions a query looks at:
+//   full   : [0, N_t)                                       (dense / tau = 1)
+//   focal  : [0, N_t), plus image-token logits for scoring  (FastOCR,
+//            Focal-Guided Pruning: focal layers see the whole cache)
+//   sparse : [0, start) ++ selected image positions ++ [start+N_img, N_t)
+//            (FastOCR, cross-layer propagation / Cross-Step Fixation Reuse)
+//   rswa   : [0, L_m) ++ [max(L_m, N_t - n), N_t)           (Unlimited OCR, R-SWA)
+//
+// Work decomposition (split-K flash-decode): grid = (splits, H_kv, B). A CTA
+// owns one KV head of one sequence and a contiguous slice of the attend list;
+// its four warps stream 16-token tiles of that slice independently through a
+// 3-stage cp.async pipeline (16-byte chunks, XOR-swizzled rows, so any
+// gathered row is a coalesced 256-byte read and ldmatrix is conflict-free).
+// For bf16 the GQA group (g <= 8 query heads) x 16 keys contraction and the
+// P.V product run on the tensor cores (mma.sync m16n8k16, keys/head-dim on M,
+// query heads on N); fp32 runs on the CUDA cores. Softmax is online in the
+// base-2 domain. The last CTA to finish a (sequence, KV head) merges the
+// split partials (no spin-waits: an atomic ticket decides who merges). In
+// focal mode that CTA also turns its group's logits into probabilities
+// summed over its query heads, and the last KV-head CTA of the sequence sums
+// the groups and runs a radix select for the top k (ties to the lower
+// position), writing the selection without a host round trip.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fastocr {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kTile = 16;      // tokens per warp tile
+constexpr int kSlots = 8;      // query-head slots per KV head (g <= 8)
+constexpr int kStages = 3;     // cp.async pipeline depth per warp
+constexpr int kMaxSplits = 64;
+constexpr int kMaxImg = 16384; // image tokens whose scores fit in shared memory
+
+enum Mode : int { kFull = 0, kFocal = 1, kSparse = 2, kRswa = 3 };
+
+// device status bits (same values as FASTOCR_DEV_* in fastocr.h)
+constexpr int kDevBadPage = 1;
+constexpr int kDevBadSeqLen = 2;
+constexpr int kDevBadImg = 4;
+constexpr int kDevBadSelection = 8;
+
+struct Params {
+  const void* q;
+  void* out;
+  const void* k;
+  const void* v;
+  const int32_t* block_table;
+  const int32_t* seq_len;
+  int num_pages, max_pages, log2_page;
+  int B, Hq, Hkv, g;
+  // index sets
+  const int32_t* img_range;  // [B,2] focal / sparse
+  const int32_t* idx;        // sparse: selected positions
+  int idx_stride;
+  const int32_t* k_in;       // sparse: [B]
+  int32_t* idx_out;          // focal: [B, idx_stride]
+  int32_t* k_out;            // focal: [B]
+  double tau;
+  int prefix_len, window;    // rswa
+  int splits;
+  float scale_log2;          // log2(e) / sqrt(d)
+  // workspace
+  float* part_ml;            // [B, H_kv, kMaxSplits, kSlots, 2]
+  float* part_acc;           // [B, H_kv, kMaxSplits, kSlots, D]
+  float* logits;             // [B, H_kv, max_img, kSlots]
+  float* sigma_part;         // [B, H_kv, max_img]
+  int32_t* cnt_head;         // [B * H_kv]
+  int32_t* cnt_seq;          // [B]
+  double* profile;           // [num_layers]
+  int profile_layer;
+  int32_t* status;
+  int max_img;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t r[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t r[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+// D(16x8, f32) += A(16x16, bf16, row) * B(16x8, bf16, col)
+__device__ __forceinline__ void mma_bf16(float c[4], const uint32_t a[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
+      "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// 2^x on the special-function unit (x = -inf gives +0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Keep count k = ceil(tau * n - 1e-9) in IEEE double, clamped to [1, n];
+// explicit round-to-nearest intrinsics keep the compiler from fusing the
+// multiply and subtract, so host, device and any IEEE double evaluation agree.
+__host__ __device__ inline int keep_count(double tau, int n) {
+  if (n <= 0) return 0;
+#ifdef __CUDA_ARCH__
+  double x = __dsub_rn(__dmul_rn(tau, (double)n), 1e-9);
+#else
+  volatile double prod = tau * (double)n;
+  volatile double x = prod - 1e-9;
+#endif
+  double c = ceil(x);
+  int k = c < 1.0 ? 1 : (c > (double)n ? n : (int)c);
+  return k;
+}
+
+// ---------------------------------------------------------------- attend list
+
+struct AttendList {
+  int n_t;
+  int n_pre;             // positions [0, n_pre)
+  const int32_t* sel;    // then sel[0 .. n_sel)
+  int n_sel;
+  int tail_start;        // then tail_start + [0, n_att - n_pre - n_sel)
+  int n_att;
+  int img_start, n_img;  // image range (focal: logits; sparse: selection check)
+};
+
+template <int MODE>
+__device__ __forceinline__ AttendList make_list(const Params& p, int b, int& bad) {
+  AttendList L;
+  const int cap = p.max_pages << p.log2_page;
+  int n_t = __ldg(p.seq_len + b);
+  if (n_t < 1 || n_t > cap) {
+    bad |= kDevBadSeqLen;
+    n_t = n_t < 0 ? 0 : (n_t > cap ? cap : n_t);
+  }
+  L.n_t = n_t;
+  L.sel = nullptr;
+  L.n_sel = 0;
+  L.tail_start = 0;
+  L.img_start = 0;
+  L.n_img = 0;
+  if (MODE == kFocal || MODE == kSparse) {
+    int s = __ldg(p.img_range + 2 * b), n = __ldg(p.img_range + 2 * b + 1);
+    if (s < 0 || n < 0 || s > n_t || n > n_t - s || (MODE == kFocal && n > p.max_img)) {
+      bad |= kDevBadImg;
+      s = s < 0 ? 0 : (s > n_t ? n_t : s);
+      n = n < 0 ? 0 : (n > n_t - s ? n_t - s : n);
+      if (MODE == kFocal && n > p.max_img) n = p.max_img;
+    }
+    L.img_start = s;
+    L.n_img = n;
+  }
+  if (MODE == kFull || MODE == kFocal) {
+    L.n_pre = n_t;
+    L.n_att = n_t;
+  } else if (MODE == kSparse) {
+    int k = __ldg(p.k_in + b);
+    const int k_cap = L.n_img < p.idx_stride ? L.n_img : p.idx_stride;
+    if (k < 0 || k > k_cap) {
+      bad |= kDevBadSelection;
+      k = k < 0 ? 0 : k_cap;
+    }
+    L.n_pre = L.img_start;
+    L.sel = p.idx + (size_t)b * p.idx_stride;
+    L.n_sel = k;
+    L.tail_start = L.img_start + L.n_img;
+    L.n_att = L.n_pre + k + (n_t - L.tail_start);
+  } else {  // kRswa
+    L.n_pre = p.prefix_len < n_t ? p.prefix_len : n_t;
+    int ts = n_t - p.window;
+    L.tail_start = ts > p.prefix_len ? ts : p.prefix_len;
+    int n_tail = n_t - L.tail_start;
+    L.n_att = L.n_pre + (n_tail > 0 ? n_tail : 0);
+  }
+  return L;
+}
+
+// Cache position of list entry v, or -1 (masked) if it is invalid.
+template <int MODE>
+__device__ __forceinline__ int list_pos(const AttendList& L, int v, int& bad) {
+  if (v < L.n_pre) return v;
+  v -= L.n_pre;
+  if (MODE == kSparse) {
+    if (v < L.n_sel) {
+      int pos = __ldg(L.sel + v);
+      if (pos < L.img_start || pos >= L.img_start + L.n_img) {
+        bad |= kDevBadSelection;
+        return -1;
+      }
+      return pos;
+    }
+    v -= L.n_sel;
+  }
+  return L.tail_start + v;
+}
+
+// ---------------------------------------------------------------- shared memory
+
+template <typename T, int D>
+struct Smem {
+  static constexpr int kRowBytes = D * (int)sizeof(T);
+  static constexpr int kStageBytes = 2 * kTile * kRowBytes;          // K rows then V rows
+  static constexpr int kPipeBytes = kWarps * kStages * kStageBytes;
+  static constexpr int kPosOffset = kPipeBytes;                      // int pos[W][S][16]
+  static constexpr int kQOffset = kPosOffset + kWarps * kStages * kTile * 4;  // f32 q[8][D]
+  static constexpr int kMainBytes = kQOffset + kSlots * D * 4;
+};
+
+template <int D>
+struct EpiSmem {
+  // wm[W][8], wl[W][8], wacc[W][8][D], then the merge area: M[8], invL[8],
+  // scale[kMaxSplits][8], misc ints
+  static constexpr int kWm = 0;
+  static constexpr int kWl = kWm + kWarps * kSlots * 4;
+  static constexpr int kWacc = kWl + kWarps * kSlots * 4;
+  static constexpr int kM = kWacc + kWarps * kSlots * D * 4;
+  static constexpr int kInvL = kM + kSlots * 4;
+  static constexpr int kScale = kInvL + kSlots * 4;
+  static constexpr int kMisc = kScale + kMaxSplits * kSlots * 4;
+  static constexpr int kBytes = kMisc + 64;
+};
+
+struct TopkSmem {
+  // keys[max_img] (uint32), then hist[256] at a 16-byte boundary, then 64
+  // ints of scan scratch (the upper half also holds kWarps doubles)
+  __host__ __device__ static int hist_offset(int max_img) { return (max_img * 4 + 15) / 16 * 16; }
+  __host__ __device__ static int bytes(int max_img) { return hist_offset(max_img) + 256 * 4 + 64 * 4; }
+};
+
+template <typename T, int D>
+inline int attend_smem_bytes(int max_img) {
+  int a = Smem<T, D>::kMainBytes;
+  int b = EpiSmem<D>::kBytes;
+  int c = TopkSmem::bytes(max_img);
+  int m = a > b ? a : b;
+  return m > c ? m : c;
+}
+
+// ---------------------------------------------------------------- warp reductions
+
+__device__ __forceinline__ float warp_max_gid(float x) {  // over lanes with equal lane%4
+  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
+  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 8));
+  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 16));
+  return x;
+}
+__device__ __forceinline__ float warp_sum_gid(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 4);
+  x += __shfl_xor_sync(0xffffffffu, x, 8);
+  x += __shfl_xor_sync(0xffffffffu, x, 16);
+  return x;
+}
+
+// Exclusive prefix sum over the CTA (kThreads threads); `scratch` holds kWarps ints.
+__device__ __forceinline__ int block_exclusive_scan(int x, int* scratch, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  __syncthreads();
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  int before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    int v = scratch[w];
+    if (w < warp) before += v;
+    all += v;
+  }
+  if (total) *total = all;
+  return before + incl - x;
+}
+
+// ---------------------------------------------------------------- per-warp state
+
+// bf16 tensor-core path: thread (gid = lane/4, tig = lane%4) owns query-head
+// slots 2*tig, 2*tig+1; accumulator O^T[d][head] as m16n8 fragments.
+template <int D>
+struct WarpStateMma {
+  float acc[D / 16][4];
+  float m[2], l[2];
+  uint32_t qf[D / 16][2];
+};
+
+// fp32 CUDA-core path: lane owns head-dim columns lane + 32*j of every slot.
+template <int D>
+struct WarpStateF32 {
+  float acc[kSlots][D / 32];
+  float m[kSlots], l[kSlots];
+};
+
+}  // namespace fastocr

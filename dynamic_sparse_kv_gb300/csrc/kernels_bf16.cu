@@ -1,0 +1,24 @@
+// bf16 instances of the decode-attention kernel (tensor-core GQA contraction).
+#include "attend_impl.cuh"
+
+namespace fastocr {
+
+cudaError_t launch_bf16(int head_dim, int mode, const Params& p, cudaStream_t s) {
+  switch (head_dim) {
+    case 64: return dispatch_mode<__nv_bfloat16, 64>(mode, p, s);
+    case 128: return dispatch_mode<__nv_bfloat16, 128>(mode, p, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+int smem_bytes_bf16(int head_dim, int max_img) {
+  return head_dim == 64 ? attend_smem_bytes<__nv_bfloat16, 64>(max_img)
+                        : attend_smem_bytes<__nv_bfloat16, 128>(max_img);
+}
+
+cudaError_t prepare_bf16() {
+  cudaError_t e = prepare_all_modes<__nv_bfloat16, 64>();
+  return e != cudaSuccess ? e : prepare_all_modes<__nv_bfloat16, 128>();
+}
+
+}  // namespace fastocr

@@ -1,0 +1,188 @@
+"""Per-step schedule of FastOCR decode attention over the C ABI.
+
+FastOCR (gist.science technical summary, "Focal-Guided Pruning" and
+"Cross-Step Fixation Reuse"):
+  * warm-up: w steps of full attention in every layer while the library
+    accumulates each layer's image-attention mass; the |C| layers with the
+    most image mass become the focal set C (fastocr_profiler_select);
+  * each later step: layers in C call fastocr_focal_attend (full cache,
+    head-summed image scores, top ceil(tau*N_img)); the selection is handed
+    to the following non-focal layers (fastocr_sparse_attend);
+  * non-focal layers before the first focal layer reuse F_last, the previous
+    step's selection of the deepest focal layer.
+Unlimited OCR (R-SWA): every layer calls fastocr_rswa_attend.
+
+The selection never leaves the GPU: every focal layer writes into its own
+fixed device buffer, and F_last *is* the deepest focal layer's buffer, which
+that layer overwrites only after all of this step's earlier readers ran. All
+buffers have fixed addresses, so a whole step can be captured in a CUDA
+graph and replayed (fastocr calls allocate nothing).
+
+This module only sequences library calls; all arithmetic is in the kernels.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _native as N
+
+
+def keep_capacity(tau: float, n_img: int) -> int:
+    """Columns needed for a selection buffer: an upper bound of ceil(tau*N_img)."""
+    return max(1, min(n_img, int(math.ceil(tau * n_img)) + 1)) if n_img > 0 else 1
+
+
+class DecodeAttention:
+    """Decode attention of a stack of layers over a paged KV cache.
+
+    k_cache, v_cache: [layers, num_pages, H_kv, page_size, d] (bf16 or fp32)
+    block_table: [B, pages_per_seq] int32; img_range: [B, 2] int32 (focal modes).
+    """
+
+    def __init__(self, k_cache, v_cache, block_table, *, q_heads: int, img_range=None,
+                 max_img: int = 0, tau: float = 1.0, mode: str = "fastocr",
+                 rswa_prefix: int = 0, rswa_window: int = 0, splits=None):
+        assert k_cache.is_cuda and k_cache.shape == v_cache.shape
+        self.k_cache, self.v_cache = k_cache, v_cache
+        self.layers, self.num_pages, self.kv_heads, self.page_size, self.head_dim = k_cache.shape
+        self.batch = block_table.shape[0]
+        self.q_heads = q_heads
+        self.mode = mode
+        self.tau = float(tau)
+        self.rswa_prefix, self.rswa_window = rswa_prefix, rswa_window
+        dev = k_cache.device
+        self.block_table = block_table.to(device=dev, dtype=torch.int32).contiguous()
+        self.img_range = (img_range.to(device=dev, dtype=torch.int32).contiguous()
+                          if img_range is not None else None)
+        self.max_img = int(max_img)
+        dtype = N.FASTOCR_DTYPE_BF16 if k_cache.dtype == torch.bfloat16 else N.FASTOCR_DTYPE_F32
+        self.handle = N.fastocr_create(self.batch, q_heads, self.kv_heads, self.head_dim, dtype,
+                                       self.page_size, self.block_table.shape[1], self.max_img,
+                                       self.layers)
+        if splits:
+            for m, s in splits.items():
+                N.fastocr_set_splits(self.handle, m, s)
+        self.seq_len = torch.zeros(self.batch, dtype=torch.int32, device=dev)
+        self.kv = [N.make_kv(k_cache[l], v_cache[l], self.block_table, self.seq_len)
+                   for l in range(self.layers)]
+        self.stride = keep_capacity(self.tau, self.max_img)
+        self.focal: tuple = ()
+        self.sel = {}          # focal layer -> (idx [B, stride], k [B])
+        self.warm_idx = None   # [layers, B, stride] selections made during warm-up
+        self.warm_k = None
+        self.has_f_last = False
+
+    def close(self):
+        if self.handle:
+            N.fastocr_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ------------------------------------------------------------ set-up
+    def set_seq_len(self, n_t):
+        """N_t of the current step, int (all sequences) or [B] tensor."""
+        if isinstance(n_t, int):
+            self.seq_len.fill_(n_t)
+        else:
+            self.seq_len.copy_(n_t, non_blocking=True)
+
+    def set_focal_layers(self, focal):
+        self.focal = tuple(sorted(int(l) for l in focal))
+        dev = self.k_cache.device
+        self.sel = {l: (torch.zeros(self.batch, self.stride, dtype=torch.int32, device=dev),
+                        torch.zeros(self.batch, dtype=torch.int32, device=dev))
+                    for l in self.focal}
+
+    def begin_warmup(self, stream=None):
+        dev = self.k_cache.device
+        self.warm_idx = torch.zeros(self.layers, self.batch, self.stride, dtype=torch.int32,
+                                    device=dev)
+        self.warm_k = torch.zeros(self.layers, self.batch, dtype=torch.int32, device=dev)
+        N.fastocr_profiler_reset(self.handle, stream)
+
+    def warmup_step(self, q, out, stream=None):
+        """Full attention in every layer, profiling image mass; keeps every layer's
+        selection so that F_last can be taken once C is known."""
+        for l in range(self.layers):
+            N.fastocr_focal_attend(self.handle, q[l], self.kv[l], self.img_range, self.tau,
+                                   out[l], self.warm_idx[l], self.stride, self.warm_k[l],
+                                   profile_layer=l, stream=stream)
+
+    def finish_warmup(self, n_focal: int, stream=None):
+        """Choose C from the profile; F_last = last warm-up selection of max(C)."""
+        focal, mass = N.fastocr_profiler_select(self.handle, n_focal, self.layers, stream)
+        self.set_focal_layers(focal)
+        deepest = max(self.focal)
+        idx, k = self.sel[deepest]
+        idx.copy_(self.warm_idx[deepest])
+        k.copy_(self.warm_k[deepest])
+        self.has_f_last = True
+        return focal, mass
+
+    # ------------------------------------------------------------ steps
+    def step(self, q, out, stream=None):
+        """One steady FastOCR decode step over all layers (q, out: [L, B, H_q, d])."""
+        cur = self.sel[max(self.focal)] if self.has_f_last else None
+        for l in range(self.layers):
+            if l in self.sel:
+                idx, k = self.sel[l]
+                N.fastocr_focal_attend(self.handle, q[l], self.kv[l], self.img_range, self.tau,
+                                       out[l], idx, self.stride, k, -1, stream)
+                cur = (idx, k)
+            elif cur is None:
+                N.fastocr_full_attend(self.handle, q[l], self.kv[l], out[l], stream)
+            else:
+                N.fastocr_sparse_attend(self.handle, q[l], self.kv[l], self.img_range, cur[0],
+                                        self.stride, cur[1], out[l], stream)
+        self.has_f_last = True
+
+    def dense_step(self, q, out, stream=None):
+        for l in range(self.layers):
+            N.fastocr_full_attend(self.handle, q[l], self.kv[l], out[l], stream)
+
+    def rswa_step(self, q, out, stream=None):
+        for l in range(self.layers):
+            N.fastocr_rswa_attend(self.handle, q[l], self.kv[l], self.rswa_prefix,
+                                  self.rswa_window, out[l], stream)
+
+    def launches_per_step(self, kind: str) -> int:
+        return self.layers
+
+    def device_status(self, stream=None) -> int:
+        return N.fastocr_device_status(self.handle, stream)
+
+
+class CapturedStep:
+    """One decode step of `dec` captured in a CUDA graph over static buffers.
+
+    q, out: [L, B, H_q, d] device tensors owned by this object; write the
+    step's queries into q (and N_t into dec.seq_len), then replay(). kind:
+    "fastocr" (steady FastOCR step), "dense" (full attention in every layer)
+    or "rswa".
+    """
+
+    def __init__(self, dec: DecodeAttention, kind: str = "fastocr"):
+        self.dec, self.kind = dec, kind
+        shape = (dec.layers, dec.batch, dec.q_heads, dec.head_dim)
+        self.q = torch.zeros(shape, dtype=dec.k_cache.dtype, device=dec.k_cache.device)
+        self.out = torch.zeros_like(self.q)
+        fn = {"fastocr": dec.step, "dense": dec.dense_step, "rswa": dec.rswa_step}[kind]
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn(self.q, self.out)             # warm run outside the capture
+        torch.cuda.current_stream().wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            fn(self.q, self.out)
+        self.launches = dec.layers           # one kernel per layer call
+
+    def replay(self):
+        self.graph.replay()

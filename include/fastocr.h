@@ -1,0 +1,187 @@
+/*
+ * fastocr.h -- C ABI of libfastocr.so: decode attention of FastOCR
+ * (focal layers with image-token selection, non-focal gather attention,
+ * Cross-Step Fixation Reuse) and of R-SWA, over a paged, never-evicted
+ * KV cache, on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources:
+ *  [FGP]   FastOCR: Dynamic Visual Fixation via KV Cache Pruning for Efficient
+ *          Document Parsing -- technical summary (gist.science), section
+ *          "Focal-Guided Pruning": focal layers attend to the full KV cache and
+ *          pick the most-attended image tokens at keep ratio tau; the
+ *          selection is propagated to every non-focal layer, which attends only
+ *          to the pruned set. Focal layers are found by profiling each layer's
+ *          image-attention ratio over a warm-up of w steps.
+ *  [CSFR]  same page, section "Cross-Step Fixation Reuse": non-focal layers
+ *          before the first focal layer start from F_last, the previous step's
+ *          selection of the deepest focal layer.
+ *  [RSWA]  Unlimited OCR summary (my-wiki-6fu.pages.dev), R-SWA paragraph:
+ *          attention limited to a global prefix (visual + prompt tokens) and a
+ *          causal sliding window of width n (default 128) over generated text.
+ *  [ABS]   FastOCR abstract: the full cache is kept; which tokens are attended
+ *          changes per step (no eviction).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  B sequences, H_q query heads, H_kv KV heads (H_q % H_kv == 0 and
+ *  g = H_q / H_kv <= 8), head dimension d (64 or 128). Query head h reads
+ *  KV head h / g. Softmax scale 1/sqrt(d).
+ *  dtype: FASTOCR_DTYPE_BF16 (q, K, V, out in bf16; fp32 accumulation) or
+ *         FASTOCR_DTYPE_F32 (all fp32, CUDA-core arithmetic, no TF32).
+ *  q, out:        [B, H_q, d] contiguous, device memory, caller-owned.
+ *  K, V caches:   [num_pages, H_kv, page_size, d] contiguous per layer, device.
+ *  block_table:   [B, max_pages_per_seq] int32, device; page of token p of
+ *                 sequence b is block_table[b][p / page_size], row p % page_size.
+ *  seq_len:       [B] int32, device; N_t = tokens in the cache, the current
+ *                 decode token included (its K/V already written).
+ *  img_range:     [B, 2] int32, device; (start, N_img) of the image tokens.
+ *                 Text prefix = [0, start); generated = [start + N_img, N_t).
+ *  Image scores (focal layers) are the probabilities of the layer's softmax
+ *  over the whole cache, summed over all H_q query heads; k = ceil(tau*N_img)
+ *  (IEEE double, ceil(tau*N_img - 1e-9), clamped to [1, N_img]); ties go to
+ *  the lower position; selections are absolute positions, ascending.
+ *
+ *  Every compute call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *  legacy default stream), allocates nothing and never synchronises, so a
+ *  sequence of calls can be captured in a CUDA graph. Calls that share a
+ *  handle must be ordered (one stream, or events): the handle's workspace is
+ *  reused by every call.
+ *
+ *  Errors: argument errors are detected on the host and returned as a
+ *  negative status before anything is launched. Faults in device data (page
+ *  id out of range, seq_len above capacity, selection outside the image,
+ *  bad image range) never trap: the kernel masks the offending token, ORs a
+ *  FASTOCR_DEV_* bit into the handle's device status word and goes on;
+ *  read and clear it with fastocr_device_status().
+ */
+#ifndef FASTOCR_H
+#define FASTOCR_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FASTOCR_ABI_VERSION 1
+
+typedef struct fastocr_handle fastocr_handle;
+typedef void* fastocr_stream; /* cudaStream_t */
+
+typedef enum {
+  FASTOCR_OK = 0,
+  FASTOCR_ERR_NULL = -1,        /* a required pointer is NULL */
+  FASTOCR_ERR_INVALID = -2,     /* a size / ratio / layer id is out of range */
+  FASTOCR_ERR_UNSUPPORTED = -3, /* shape outside what the kernels implement */
+  FASTOCR_ERR_CUDA = -4,        /* a CUDA runtime call failed */
+  FASTOCR_ERR_NO_DEVICE = -5,   /* no usable sm_103 device */
+  FASTOCR_ERR_ALIGN = -6        /* a device pointer is not 16-byte aligned */
+} fastocr_status;
+
+typedef enum { FASTOCR_DTYPE_F32 = 0, FASTOCR_DTYPE_BF16 = 1 } fastocr_dtype;
+
+/* Device status bits (fastocr_device_status). */
+#define FASTOCR_DEV_BAD_PAGE 1      /* block_table entry outside [0, num_pages) */
+#define FASTOCR_DEV_BAD_SEQLEN 2    /* seq_len < 1 or above max_pages_per_seq*page_size */
+#define FASTOCR_DEV_BAD_IMG 4       /* img_range outside [0, N_t) */
+#define FASTOCR_DEV_BAD_SELECTION 8 /* selected position outside the image, or k > N_img */
+
+/* Shapes fixed for the life of a handle. */
+typedef struct {
+  int32_t batch;             /* B >= 1 */
+  int32_t num_q_heads;       /* H_q */
+  int32_t num_kv_heads;      /* H_kv; H_q % H_kv == 0, H_q / H_kv <= 8 */
+  int32_t head_dim;          /* d: 64 or 128 */
+  int32_t dtype;             /* fastocr_dtype */
+  int32_t page_size;         /* tokens per page: power of two, 1..256 */
+  int32_t max_pages_per_seq; /* columns of block_table */
+  int32_t max_img_tokens;    /* upper bound of N_img (<= 16384); 0 if no focal calls */
+  int32_t num_layers;        /* profiler slots (>= 1) */
+} fastocr_dims;
+
+/* One layer's KV cache (all pointers device memory, caller-owned). */
+typedef struct {
+  const void* k;              /* [num_pages, H_kv, page_size, d] */
+  const void* v;              /* [num_pages, H_kv, page_size, d] */
+  const int32_t* block_table; /* [B, max_pages_per_seq] */
+  const int32_t* seq_len;     /* [B] */
+  int32_t num_pages;          /* pages in k and v (bounds check) */
+} fastocr_kv;
+
+/* Library and ABI version; never fails, needs no GPU. */
+int32_t fastocr_abi_version(void);
+
+/* Human-readable text of a fastocr_status; never NULL, needs no GPU. */
+const char* fastocr_status_string(int32_t status);
+
+/* Create a handle for the current CUDA device: checks dims, allocates the
+ * workspace (split partials, focal logits, scores, counters, profiler
+ * accumulator, device status word) once. *out is set only on FASTOCR_OK.
+ * Synchronous. Errors: NULL, INVALID, UNSUPPORTED, NO_DEVICE, CUDA. */
+fastocr_status fastocr_create(const fastocr_dims* dims, fastocr_handle** out);
+
+/* Free the handle and its workspace (synchronises the device first).
+ * NULL is accepted and ignored. */
+fastocr_status fastocr_destroy(fastocr_handle* h);
+
+/* Full decode attention over [0, N_t) for every sequence -- the dense / tau=1
+ * baseline layer. [FGP] (what focal layers compute, without selection). */
+fastocr_status fastocr_full_attend(fastocr_handle* h, const void* q, const fastocr_kv* kv,
+                                   void* out, fastocr_stream stream);
+
+/* Focal layer [FGP]: full decode attention over [0, N_t), image scores
+ * (head-summed probabilities of image tokens), and the top
+ * k_b = ceil(tau*N_img_b) image tokens of every sequence, written to
+ * idx[b*idx_stride + 0 .. k_b-1] as ascending absolute positions, with k_b in
+ * k_out[b]. Scoring and selection run on the device (no host round trip).
+ * tau in (0, 1]; idx_stride >= ceil(tau*max_img_tokens).
+ * profile_layer >= 0 (< num_layers) adds the image probability mass summed
+ * over sequences and query heads to that layer's profiler slot (warm-up);
+ * -1 disables profiling. */
+fastocr_status fastocr_focal_attend(fastocr_handle* h, const void* q, const fastocr_kv* kv,
+                                    const int32_t* img_range, double tau, void* out,
+                                    int32_t* idx, int32_t idx_stride, int32_t* k_out,
+                                    int32_t profile_layer, fastocr_stream stream);
+
+/* Non-focal layer [FGP, CSFR]: attention over the text prefix [0, start),
+ * the k[b] selected image positions idx[b*idx_stride + 0 .. k[b]-1] (any
+ * order, each inside the image range), and the generated tokens
+ * [start + N_img, N_t). Passing F_last (the previous step's selection of the
+ * deepest focal layer) here is Cross-Step Fixation Reuse. */
+fastocr_status fastocr_sparse_attend(fastocr_handle* h, const void* q, const fastocr_kv* kv,
+                                     const int32_t* img_range, const int32_t* idx,
+                                     int32_t idx_stride, const int32_t* k, void* out,
+                                     fastocr_stream stream);
+
+/* R-SWA layer [RSWA]: attention over [0, prefix_len) and the last `window`
+ * tokens of [prefix_len, N_t), the current token included. prefix_len >= 0,
+ * window >= 0. */
+fastocr_status fastocr_rswa_attend(fastocr_handle* h, const void* q, const fastocr_kv* kv,
+                                   int32_t prefix_len, int32_t window, void* out,
+                                   fastocr_stream stream);
+
+/* Zero the profiler accumulator of every layer (asynchronous on stream). */
+fastocr_status fastocr_profiler_reset(fastocr_handle* h, fastocr_stream stream);
+
+/* Focal layer selection [FGP]: read the accumulated image-attention mass of
+ * every layer (synchronises `stream`), write the n_focal layers with the
+ * largest mass (ties: lower layer id) in ascending order to layers_out
+ * (host, n_focal entries) and, if ratio_out is not NULL, the mass of every
+ * layer to ratio_out (host, num_layers entries). 1 <= n_focal <= num_layers. */
+fastocr_status fastocr_profiler_select(fastocr_handle* h, int32_t n_focal, int32_t* layers_out,
+                                       double* ratio_out, fastocr_stream stream);
+
+/* Read the device status word (FASTOCR_DEV_* bits, 0 = clean) into *status
+ * (host) and clear it. Synchronises `stream`. */
+fastocr_status fastocr_device_status(fastocr_handle* h, int32_t* status, fastocr_stream stream);
+
+/* Override the split-K factor of a mode (0 = full/focal, 1 = sparse,
+ * 2 = R-SWA); 0 restores the automatic choice. Splits are clamped to
+ * [1, 64]. */
+fastocr_status fastocr_set_splits(fastocr_handle* h, int32_t mode, int32_t splits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FASTOCR_H */

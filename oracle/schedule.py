@@ -41,11 +41,13 @@ def choose_focal_layers(ratio, n_focal: int):
     return tuple(sorted(order[:n_focal]))
 
 
-def warmup_step(q_step, kv, n_t, img, tau):
+def warmup_step(q_step, kv, n_t, img, tau, accept=None):
     """One warm-up step: every layer attends to the whole cache.
 
     q_step: [L, B, H_q, d]; kv(layer, b) -> (K, V) logical [>= n_t[b], H_kv, d];
     n_t: [B]; img: [B, 2] (start, N_img).
+    accept(l, b, selection, sigma) -> selection lets a caller continue with
+    another valid selection of the same scores (see steady_step).
     Returns (outs [L, B, H_q, d], image mass per layer [L] summed over sequences
     and heads, selection of every layer [L][B])."""
     q_step = np.asarray(q_step, dtype=np.float64)
@@ -60,15 +62,20 @@ def warmup_step(q_step, kv, n_t, img, tau):
             out, s, sigma = A.focal_attend(q_step[l, b], K, V, int(n_t[b]), start, n_img, tau)
             outs[l, b] = out
             mass[l] += sigma.sum()
-            sel[l][b] = s
+            sel[l][b] = accept(l, b, s, sigma) if accept else s
     return outs, mass, sel
 
 
-def steady_step(q_step, kv, n_t, img, tau, focal, f_last):
+def steady_step(q_step, kv, n_t, img, tau, focal, f_last, accept=None):
     """One decode step after warm-up.
 
     focal: the focal layer ids C; f_last: [B] selections of the previous step
-    (None entries: no selection yet). Returns (outs [L, B, H_q, d],
+    (None entries: no selection yet). accept(l, b, selection, sigma), if
+    given, returns the selection the step continues with: a parity test uses
+    it to continue with the GPU's selection once it has checked that it is a
+    valid top-k of these scores (ties within tolerance), so that one allowed
+    swap at the boundary does not change every later comparison.
+    Returns (outs [L, B, H_q, d],
     selection used or made by each layer [L][B], new F_last [B])."""
     q_step = np.asarray(q_step, dtype=np.float64)
     n_layers, batch, n_q, d = q_step.shape
@@ -81,8 +88,8 @@ def steady_step(q_step, kv, n_t, img, tau, focal, f_last):
             K, V = kv(l, b)
             start, n_img = int(img[b][0]), int(img[b][1])
             if l in focal:
-                out, s, _ = A.focal_attend(q_step[l, b], K, V, int(n_t[b]), start, n_img, tau)
-                current[b] = s
+                out, s, sigma = A.focal_attend(q_step[l, b], K, V, int(n_t[b]), start, n_img, tau)
+                current[b] = accept(l, b, s, sigma) if accept else s
             elif current[b] is None:
                 out = A.full_attend(q_step[l, b], K, V, int(n_t[b]))
             else:
@@ -93,10 +100,11 @@ def steady_step(q_step, kv, n_t, img, tau, focal, f_last):
 
 
 def run_decode(q_of, kv_of, n_t_of, img, tau, n_layers, batch, n_q, steps, warmup=0,
-               n_focal=3, focal_layers=None):
+               n_focal=3, focal_layers=None, accept=None):
     """Whole schedule over decode steps 0 .. steps-1.
 
-    q_of(t) -> [L, B, H_q, d]; kv_of(t) -> kv(layer, b); n_t_of(t) -> [B].
+    q_of(t) -> [L, B, H_q, d]; kv_of(t) -> kv(layer, b); n_t_of(t) -> [B];
+    accept(t, l, b, selection, sigma) as in steady_step.
     Returns dict(outs=[steps] arrays, used=[steps][L][B], focal=C, ratio=[L])."""
     ratio = np.zeros(n_layers)
     focal = tuple(focal_layers) if focal_layers is not None else None
@@ -104,8 +112,9 @@ def run_decode(q_of, kv_of, n_t_of, img, tau, n_layers, batch, n_q, steps, warmu
     outs, used = [], []
     for t in range(steps):
         q_step, kv, n_t = q_of(t), kv_of(t), n_t_of(t)
+        acc = (lambda l, b, s, sg, t=t: accept(t, l, b, s, sg)) if accept else None
         if t < warmup:
-            o, mass, sel = warmup_step(q_step, kv, n_t, img, tau)
+            o, mass, sel = warmup_step(q_step, kv, n_t, img, tau, acc)
             ratio += mass / (warmup * batch * n_q)
             outs.append(o)
             used.append([[None] * batch for _ in range(n_layers)])
@@ -114,7 +123,7 @@ def run_decode(q_of, kv_of, n_t_of, img, tau, n_layers, batch, n_q, steps, warmu
                     focal = choose_focal_layers(ratio, n_focal)
                 f_last = list(sel[max(focal)])
         else:
-            o, u, f_last = steady_step(q_step, kv, n_t, img, tau, focal, f_last)
+            o, u, f_last = steady_step(q_step, kv, n_t, img, tau, focal, f_last, acc)
             outs.append(o)
             used.append(u)
     return dict(outs=outs, used=used, focal=focal, ratio=ratio, f_last=f_last)

@@ -1,0 +1,86 @@
+"""The C-ABI library builds, loads and exports every declared entry point;
+host-side argument checks answer without touching a GPU (no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fastocr.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fastocr_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dynamic_sparse_kv_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ["fastocr_focal_attend", "fastocr_sparse_attend", "fastocr_rswa_attend",
+                 "fastocr_full_attend", "fastocr_profiler_select", "fastocr_create"]:
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    from dynamic_sparse_kv_gb300 import _native as N
+    assert N.fastocr_abi_version() == 1
+    for s in (0, -1, -2, -3, -4, -5, -6):
+        assert N.status_string(s) and N.status_string(s) != "unknown status"
+    assert N.status_string(123) == "unknown status"
+
+
+def test_host_checks_without_gpu(lib):
+    from dynamic_sparse_kv_gb300 import _native as N
+    L = N.lib
+    h = ctypes.c_void_p()
+    assert L.fastocr_create(None, ctypes.byref(h)) == N.FASTOCR_ERR_NULL
+    bad = [
+        N.fastocr_dims(0, 4, 2, 64, 1, 16, 8, 64, 2),      # batch 0
+        N.fastocr_dims(1, 6, 4, 64, 1, 16, 8, 64, 2),      # H_q % H_kv
+        N.fastocr_dims(1, 4, 2, 64, 7, 16, 8, 64, 2),      # dtype
+        N.fastocr_dims(1, 4, 2, 64, 1, 12, 8, 64, 2),      # page size not a power of 2
+        N.fastocr_dims(1, 4, 2, 64, 1, 16, 8, 64, 0),      # no layers
+    ]
+    for d in bad:
+        assert L.fastocr_create(ctypes.byref(d), ctypes.byref(h)) == N.FASTOCR_ERR_INVALID
+    unsupported = [
+        N.fastocr_dims(1, 18, 2, 64, 1, 16, 8, 64, 2),     # group 9 > 8
+        N.fastocr_dims(1, 4, 2, 96, 1, 16, 8, 64, 2),      # d = 96
+        N.fastocr_dims(1, 4, 2, 64, 1, 16, 8, 20000, 2),   # too many image tokens
+    ]
+    for d in unsupported:
+        assert L.fastocr_create(ctypes.byref(d), ctypes.byref(h)) == N.FASTOCR_ERR_UNSUPPORTED
+    # NULL handle / pointers are refused before any CUDA call
+    kv = N.fastocr_kv(None, None, None, None, 1)
+    assert L.fastocr_full_attend(None, None, ctypes.byref(kv), None, None) == N.FASTOCR_ERR_NULL
+    assert L.fastocr_sparse_attend(None, None, ctypes.byref(kv), None, None, 1, None, None,
+                                   None) == N.FASTOCR_ERR_NULL
+    assert L.fastocr_rswa_attend(None, None, ctypes.byref(kv), 0, 0, None, None) == N.FASTOCR_ERR_NULL
+    assert L.fastocr_focal_attend(None, None, ctypes.byref(kv), None, 0.5, None, None, 1, None,
+                                  -1, None) == N.FASTOCR_ERR_NULL
+    assert L.fastocr_profiler_select(None, 1, None, None, None) == N.FASTOCR_ERR_NULL
+    assert L.fastocr_destroy(None) == N.FASTOCR_OK
+
+
+def test_create_without_gpu_reports_no_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    from dynamic_sparse_kv_gb300 import _native as N
+    d = N.fastocr_dims(1, 4, 2, 64, 1, 16, 8, 64, 2)
+    h = ctypes.c_void_p()
+    assert N.lib.fastocr_create(ctypes.byref(d), ctypes.byref(h)) == N.FASTOCR_ERR_NO_DEVICE

@@ -83,7 +83,7 @@ def _choose_lowest(ratio, n_focal):
     return tuple(sorted(sorted(range(ratio.size), key=lambda l: (ratio[l], l))[:n_focal]))
 
 
-def _steady_first_focal_only(q_step, kv, n_t, img, tau, focal, f_last):
+def _steady_first_focal_only(q_step, kv, n_t, img, tau, focal, f_last, accept=None):
     # mistake: later focal layers do not replace the selection
     q_step = np.asarray(q_step, dtype=np.float64)
     n_layers, batch, n_q, d = q_step.shape

@@ -1,0 +1,234 @@
+"""CUDA path vs the CPU oracle on the same seeded inputs (GPU required).
+
+Small workloads run the whole schedule (warm-up profiling, focal selection,
+Cross-Step Fixation Reuse) and compare every output of every layer and step;
+sizes span several 16-token tiles, ragged tails, every GQA group the kernels
+support and both dtypes. Tolerances: max abs error 2e-2 for bf16 KV with
+fp32 accumulation, 1e-5 for fp32; selections exact except boundary ties
+within 1e-5 relative of the k-th score.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle.attention as A
+import synth
+from gpu_harness import TOL, GpuRun, KVCache, assert_close, check_selection, compare_decode, np64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dynamic_sparse_kv_gb300 import build
+    build.build()
+    import dynamic_sparse_kv_gb300  # noqa: F401
+
+
+def _case(name, **kw):
+    return synth.make_case(synth.workload(name, **kw), device="cuda")
+
+
+def test_tiny_f32_whole_decode():
+    """Tiny fp32 workload, all 32 steps: layer 1 focal, layer 0 reuses F_last."""
+    case = _case("tiny_f32")
+    run = GpuRun(case).run(0, case.wl.steps)
+    stats = compare_decode(run, case.wl.steps)
+    assert stats["swaps"] == 0
+
+
+@pytest.mark.parametrize("variant", [
+    dict(batch=2, layers=5, prompt=40, grid=(1, 16, 24), steps=14, warmup=3, n_focal=2),
+    dict(batch=3, layers=4, prompt=7, grid=(1, 9, 13), steps=9, warmup=2, n_focal=2, tau=0.3),
+    dict(batch=1, layers=3, prompt=64, grid=(1, 32, 32), steps=10, warmup=2, n_focal=1, tau=1.0),
+], ids=["qwen_small", "ragged", "tau1"])
+def test_qwen_shaped_decode(variant):
+    """GQA group 7, d=128, bf16, warm-up chooses C, then steady steps."""
+    case = _case("qwen7b_b1", **variant)
+    run = GpuRun(case).run(0, case.wl.steps)
+    compare_decode(run, case.wl.steps)
+
+
+@pytest.mark.parametrize("shape", [
+    dict(q_heads=10, kv_heads=10, head_dim=128),   # MHA
+    dict(q_heads=16, kv_heads=2, head_dim=128),    # group 8
+    dict(q_heads=8, kv_heads=2, head_dim=64),      # d 64
+    dict(q_heads=6, kv_heads=3, head_dim=128, dtype="f32"),
+    dict(q_heads=5, kv_heads=1, head_dim=64, dtype="f32"),
+], ids=["mha", "g8", "d64", "f32_d128", "f32_g5_d64"])
+def test_head_shapes(shape):
+    case = _case("qwen7b_b1", batch=2, layers=3, prompt=21, grid=(1, 10, 17), steps=6,
+                 warmup=2, n_focal=1, tau=0.1, **shape)
+    run = GpuRun(case).run(0, case.wl.steps)
+    compare_decode(run, case.wl.steps)
+
+
+def test_serving_shaped_random_start():
+    case = _case("serving_b32", batch=5, layers=3, prompt=37, grid=(1, 12, 20), steps=6,
+                 warmup=2, n_focal=1)
+    run = GpuRun(case).run(0, case.wl.steps)
+    compare_decode(run, case.wl.steps)
+
+
+@pytest.mark.parametrize("tau", [0.02, 0.05, 0.1, 1.0])
+def test_multipage_tau_sweep(tau):
+    case = _case("multipage_b8", batch=3, layers=3, prompt=20, grid=(4, 8, 8), steps=7,
+                 warmup=2, n_focal=2, tau=tau)
+    run = GpuRun(case).run(0, case.wl.steps)
+    compare_decode(run, case.wl.steps)
+
+
+def test_tau_one_equals_dense_on_gpu():
+    """Invariant: with tau = 1 every layer's output equals full attention."""
+    case = _case("qwen7b_b1", batch=2, layers=4, prompt=33, grid=(1, 8, 24), steps=5,
+                 warmup=2, n_focal=2, tau=1.0)
+    run = GpuRun(case).run(0, case.wl.steps)
+    dense = GpuRun(case).run(0, case.wl.steps, kind="dense")
+    for t in range(case.wl.steps):
+        d = (run.outs[t].float() - dense.outs[t].float()).abs().max().item()
+        assert d <= 2e-2, (t, d)
+        assert set(run.sels[t].keys()) <= set(range(case.wl.layers))
+
+
+def test_rswa_small():
+    """R-SWA attend set; equals full attention while T <= n."""
+    wl = synth.workload("rswa_b16", batch=3, layers=2, rswa_prefix=100, prompt=100,
+                        rswa_window=16, steps=40)
+    case = synth.make_case(wl, device="cuda")
+    run = GpuRun(case).run(0, wl.steps, kind="rswa")
+    dense = GpuRun(case).run(0, wl.steps, kind="dense")
+    kv = KVCache(case)
+    for t in range(wl.steps):
+        n_t = wl.seq_len_at(t)
+        for l in range(wl.layers):
+            for b in range(wl.batch):
+                K, V = kv(l, b)
+                ref = A.rswa_attend(np64(case.q_at(t)[l, b]), K, V, n_t, wl.rswa_prefix,
+                                    wl.rswa_window)
+                assert_close(run.outs[t][l, b], ref, TOL["bf16"], f"rswa t={t} l={l} b={b}")
+        if t + 1 <= wl.rswa_window:
+            d = (run.outs[t].float() - dense.outs[t].float()).abs().max().item()
+            assert d <= 2e-2
+
+
+def _direct(case, n_t, layer=0):
+    from dynamic_sparse_kv_gb300 import DecodeAttention
+    wl = case.wl
+    dec = DecodeAttention(case.k_cache, case.v_cache, case.block_table, q_heads=wl.q_heads,
+                          img_range=case.img_range, max_img=max(wl.n_img, 1), tau=wl.tau)
+    dec.set_seq_len(n_t)
+    return dec
+
+
+def test_constant_keys_ties_to_lowest():
+    """All keys equal -> every image token ties; the lowest k positions are kept."""
+    from dynamic_sparse_kv_gb300 import _native as N
+    case = _case("qwen7b_b1", batch=2, layers=1, prompt=19, grid=(1, 10, 10), steps=3, tau=0.13)
+    case.k_cache[:] = case.k_cache[:, :1, :1, :1, :]
+    wl = case.wl
+    n_t = wl.seq_len_at(2)
+    dec = _direct(case, n_t)
+    q = case.q_at(2)[0].contiguous()
+    out = torch.empty_like(q)
+    idx = torch.zeros(wl.batch, dec.stride, dtype=torch.int32, device="cuda")
+    k = torch.zeros(wl.batch, dtype=torch.int32, device="cuda")
+    N.fastocr_focal_attend(dec.handle, q, dec.kv[0], case.img_range, wl.tau, out, idx,
+                           dec.stride, k)
+    torch.cuda.synchronize()
+    kk = A.keep_count(wl.tau, wl.n_img)
+    assert k.tolist() == [kk] * wl.batch
+    for b in range(wl.batch):
+        assert idx[b, :kk].tolist() == list(range(wl.prompt, wl.prompt + kk))
+        Kl, Vl = KVCache(case)(0, b)
+        ref = A.full_attend(np64(q[b]), Kl, Vl, n_t)
+        assert_close(out[b], ref, TOL["bf16"])
+
+
+def test_sparse_selection_permutation_and_empty():
+    """Gather order does not matter; an empty attend list gives zeros."""
+    from dynamic_sparse_kv_gb300 import _native as N
+    case = _case("qwen7b_b1", batch=2, layers=1, prompt=0, grid=(1, 8, 8), steps=3)
+    wl = case.wl
+    n_img = wl.n_img
+    rng = np.random.default_rng(0)
+    sel = np.sort(rng.choice(n_img, 9, replace=False))
+    dec = _direct(case, wl.seq_len_at(1))
+    q = case.q_at(1)[0].contiguous()
+    outs = []
+    for order in (sel, sel[::-1].copy()):
+        idx = torch.tensor(np.tile(order, (wl.batch, 1)), dtype=torch.int32, device="cuda")
+        kk = torch.full((wl.batch,), len(order), dtype=torch.int32, device="cuda")
+        out = torch.empty_like(q)
+        N.fastocr_sparse_attend(dec.handle, q, dec.kv[0], case.img_range, idx, idx.shape[1], kk,
+                                out)
+        outs.append(out)
+    torch.cuda.synchronize()
+    for b in range(wl.batch):
+        Kl, Vl = KVCache(case)(0, b)
+        ref = A.sparse_attend(np64(q[b]), Kl, Vl, wl.seq_len_at(1), 0, n_img, sel)
+        assert_close(outs[0][b], ref, TOL["bf16"])
+        assert_close(outs[1][b], ref, TOL["bf16"])
+    # empty: no prefix, no selection, no generated tokens (seq_len = image end)
+    dec.set_seq_len(n_img)
+    idx = torch.zeros(wl.batch, 1, dtype=torch.int32, device="cuda")
+    kk = torch.zeros(wl.batch, dtype=torch.int32, device="cuda")
+    out = torch.full_like(q, 7.0)
+    N.fastocr_sparse_attend(dec.handle, q, dec.kv[0], case.img_range, idx, 1, kk, out)
+    torch.cuda.synchronize()
+    assert out.abs().max().item() == 0.0
+    assert dec.device_status() == 0
+
+
+def test_device_status_flags_bad_inputs():
+    """Bad page ids, lengths and selections are masked and reported, never fault."""
+    from dynamic_sparse_kv_gb300 import _native as N
+    case = _case("qwen7b_b1", batch=2, layers=1, prompt=16, grid=(1, 8, 8), steps=4)
+    wl = case.wl
+    dec = _direct(case, wl.seq_len_at(1))
+    q = case.q_at(1)[0].contiguous()
+    out = torch.empty_like(q)
+    bt = dec.block_table
+    saved = bt[1, 2].item()
+    bt[1, 2] = dec.num_pages + 5
+    N.fastocr_full_attend(dec.handle, q, dec.kv[0], out)
+    assert dec.device_status() & N.DEV_BAD_PAGE
+    bt[1, 2] = saved
+    dec.set_seq_len(bt.shape[1] * wl.page_size + 3)
+    N.fastocr_full_attend(dec.handle, q, dec.kv[0], out)
+    assert dec.device_status() & N.DEV_BAD_SEQLEN
+    dec.set_seq_len(wl.seq_len_at(1))
+    idx = torch.tensor([[2, 20, 30], [17, 18, 9999]], dtype=torch.int32, device="cuda")
+    kk = torch.tensor([3, 3], dtype=torch.int32, device="cuda")
+    N.fastocr_sparse_attend(dec.handle, q, dec.kv[0], case.img_range, idx, 3, kk, out)
+    assert dec.device_status() & N.DEV_BAD_SELECTION
+    kk = torch.tensor([3, 500], dtype=torch.int32, device="cuda")
+    N.fastocr_sparse_attend(dec.handle, q, dec.kv[0], case.img_range, idx, 3, kk, out)
+    assert dec.device_status() & N.DEV_BAD_SELECTION
+    N.fastocr_full_attend(dec.handle, q, dec.kv[0], out)
+    assert dec.device_status() == 0
+
+
+def test_host_argument_errors():
+    from dynamic_sparse_kv_gb300 import _native as N
+    case = _case("qwen7b_b1", batch=1, layers=1, prompt=16, grid=(1, 8, 8), steps=2)
+    dec = _direct(case, case.wl.seq_len_at(0))
+    q = case.q_at(0)[0].contiguous()
+    out = torch.empty_like(q)
+    idx = torch.zeros(1, dec.stride, dtype=torch.int32, device="cuda")
+    k = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for tau in (0.0, -0.1, 1.5, float("nan")):
+        with pytest.raises(N.FastOCRError) as e:
+            N.fastocr_focal_attend(dec.handle, q, dec.kv[0], case.img_range, tau, out, idx,
+                                   dec.stride, k)
+        assert e.value.status == N.FASTOCR_ERR_INVALID
+    with pytest.raises(N.FastOCRError) as e:
+        N.fastocr_focal_attend(dec.handle, q, dec.kv[0], case.img_range, 1.0, out, idx, 1, k)
+    assert e.value.status == N.FASTOCR_ERR_INVALID
+    with pytest.raises(N.FastOCRError) as e:
+        N.fastocr_full_attend(dec.handle, q.view(-1)[1:], dec.kv[0], out)
+    assert e.value.status == N.FASTOCR_ERR_ALIGN
+    with pytest.raises(N.FastOCRError) as e:
+        N.fastocr_rswa_attend(dec.handle, q, dec.kv[0], -1, 4, out)
+    assert e.value.status == N.FASTOCR_ERR_INVALID
