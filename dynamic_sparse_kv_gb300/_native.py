@@ -51,7 +51,7 @@ class FastOCRError(RuntimeError):
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
-            f"{LIB_PATH} is not built; run `python -m dynamic_sparse_kv_gb300.build` "
+            f"{LIB_PATH} is not built; run `python dynamic_sparse_kv_gb300/build.py` "
             "(or __graft_entry__.build()) -- there is no CPU fallback")
     lib = ctypes.CDLL(LIB_PATH)
     P, I32, F64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_double

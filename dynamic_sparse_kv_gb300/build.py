@@ -1,6 +1,6 @@
 """Build libfastocr.so in-tree with nvcc for sm_103a (no cmake, no torch extension).
 
-    python -m dynamic_sparse_kv_gb300.build [--force] [--verbose]
+    python dynamic_sparse_kv_gb300/build.py [--force] [--verbose]
 
 Translation units compile in parallel into ``_build/`` next to this file and
 link into ``libfastocr.so`` beside it, against the shared CUDA runtime (the

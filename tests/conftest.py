@@ -8,3 +8,14 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+
+
+def build_library(force=False):
+    """Build libfastocr.so (nvcc) if needed; return its path. build.py is loaded
+    by path because importing the package loads the library it builds."""
+    import importlib.util
+    path = os.path.join(ROOT, "dynamic_sparse_kv_gb300", "build.py")
+    spec = importlib.util.spec_from_file_location("_fastocr_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build(force=force)

@@ -18,9 +18,8 @@ def declared_functions():
 
 @pytest.fixture(scope="module")
 def lib():
-    from dynamic_sparse_kv_gb300 import build
-    path = build.build()
-    return ctypes.CDLL(path)
+    from conftest import build_library
+    return ctypes.CDLL(build_library())
 
 
 def test_header_declares_the_entry_points():

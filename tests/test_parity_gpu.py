@@ -22,8 +22,8 @@ pytestmark = pytest.mark.gpu
 def _lib():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    from dynamic_sparse_kv_gb300 import build
-    build.build()
+    from conftest import build_library
+    build_library()
     import dynamic_sparse_kv_gb300  # noqa: F401
 
 
