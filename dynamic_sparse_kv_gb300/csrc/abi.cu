@@ -15,6 +15,8 @@ cudaError_t launch_bf16(int head_dim, int mode, const Params& p, cudaStream_t s)
 cudaError_t launch_f32(int head_dim, int mode, const Params& p, cudaStream_t s);
 cudaError_t prepare_bf16();
 cudaError_t prepare_f32();
+int max_cluster_bf16(int head_dim);
+int max_cluster_f32(int head_dim);
 }  // namespace fastocr
 
 using namespace fastocr;
@@ -25,14 +27,11 @@ struct fastocr_handle {
   int num_sms;
   int log2_page;
   int split_override[3];
+  int max_splits;   // largest thread-block cluster the device co-schedules (<= 16)
   void* ws;
   size_t ws_bytes;
-  float* part_ml;
-  float* part_acc;
   float* logits;
   float* sigma_part;
-  int32_t* cnt_head;
-  int32_t* cnt_seq;
   double* profile;
   int32_t* status;
 };
@@ -49,13 +48,15 @@ int ilog2_exact(int x) {
   return (1 << l) == x ? l : -1;
 }
 
-// Split-K factor: minimise (waves of CTAs) / splits + a small per-split merge
-// cost, with 2 resident CTAs per SM, at most one 64-token tile per split.
+// Split-K factor (= cluster size): minimise (waves of CTAs) / splits + a small
+// per-split merge cost, with 2 resident CTAs per SM, at most one 64-token
+// tile per split, and no more splits than one cluster holds.
 int auto_splits(const fastocr_handle* h) {
   const long units = (long)h->dims.batch * h->dims.num_kv_heads;
   const long slots = (long)h->num_sms * 2;
   const long max_tokens = (long)h->dims.max_pages_per_seq << h->log2_page;
-  const int max_useful = (int)std::max(1L, std::min<long>(kMaxSplits, (max_tokens + 63) / 64));
+  const int max_useful =
+      (int)std::max(1L, std::min<long>(h->max_splits, (max_tokens + 63) / 64));
   int best = 1;
   double best_cost = 1e300;
   for (int s = 1; s <= max_useful; ++s) {
@@ -71,14 +72,16 @@ int auto_splits(const fastocr_handle* h) {
 
 int splits_for(const fastocr_handle* h, int mode_slot) {
   const int o = h->split_override[mode_slot];
-  return o > 0 ? o : auto_splits(h);
+  return o > 0 ? std::min(o, h->max_splits) : auto_splits(h);
 }
 
 fastocr_status check_kv(const fastocr_handle* h, const fastocr_kv* kv) {
   if (!kv || !kv->k || !kv->v || !kv->block_table || !kv->seq_len) return FASTOCR_ERR_NULL;
   if (kv->num_pages < 1) return FASTOCR_ERR_INVALID;
   if (!aligned16(kv->k) || !aligned16(kv->v)) return FASTOCR_ERR_ALIGN;
-  (void)h;
+  // cache rows are indexed with 32-bit integers inside the kernels
+  if ((long long)kv->num_pages * h->dims.num_kv_heads * h->dims.page_size >= (1LL << 31))
+    return FASTOCR_ERR_UNSUPPORTED;
   return FASTOCR_OK;
 }
 
@@ -100,12 +103,8 @@ Params base_params(const fastocr_handle* h, const void* q, const fastocr_kv* kv,
   p.Hkv = d.num_kv_heads;
   p.g = d.num_q_heads / d.num_kv_heads;
   p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d.head_dim));
-  p.part_ml = h->part_ml;
-  p.part_acc = h->part_acc;
   p.logits = h->logits;
   p.sigma_part = h->sigma_part;
-  p.cnt_head = h->cnt_head;
-  p.cnt_seq = h->cnt_seq;
   p.profile = h->profile;
   p.profile_layer = -1;
   p.status = h->status;
@@ -113,8 +112,12 @@ Params base_params(const fastocr_handle* h, const void* q, const fastocr_kv* kv,
   return p;
 }
 
-fastocr_status launch(const fastocr_handle* h, int mode, const Params& p, fastocr_stream stream) {
+fastocr_status launch(const fastocr_handle* h, int mode, Params p, fastocr_stream stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // small grids release the next kernel right away (its CTAs then prefetch
+  // while this one runs); grids that need the whole GPU release it only
+  // after their main loop, so its CTAs do not take slots from this grid
+  p.pdl_early = (long)p.splits * p.Hkv * p.B <= h->num_sms;
   cudaError_t e = h->dims.dtype == FASTOCR_DTYPE_BF16 ? launch_bf16(h->dims.head_dim, mode, p, s)
                                                        : launch_f32(h->dims.head_dim, mode, p, s);
   return e == cudaSuccess ? FASTOCR_OK : FASTOCR_ERR_CUDA;
@@ -164,19 +167,11 @@ fastocr_status fastocr_create(const fastocr_dims* dims, fastocr_handle** out) {
   const size_t units = (size_t)d.batch * d.num_kv_heads;
   const size_t img = (size_t)d.max_img_tokens;
   size_t off = 0;
-  const size_t o_ml = off;
-  off = align_up(off + units * kMaxSplits * kSlots * 2 * sizeof(float), 256);
-  const size_t o_acc = off;
-  off = align_up(off + units * kMaxSplits * kSlots * d.head_dim * sizeof(float), 256);
   const size_t o_logits = off;
   off = align_up(off + units * img * kSlots * sizeof(float), 256);
   const size_t o_sigma = off;
   off = align_up(off + units * img * sizeof(float), 256);
-  const size_t o_zero = off;  // counters, profiler, status: zeroed once here
-  const size_t o_cnt_head = off;
-  off = align_up(off + units * sizeof(int32_t), 256);
-  const size_t o_cnt_seq = off;
-  off = align_up(off + (size_t)d.batch * sizeof(int32_t), 256);
+  const size_t o_zero = off;  // profiler and status: zeroed once here
   const size_t o_profile = off;
   off = align_up(off + (size_t)d.num_layers * sizeof(double), 256);
   const size_t o_status = off;
@@ -188,18 +183,16 @@ fastocr_status fastocr_create(const fastocr_dims* dims, fastocr_handle** out) {
   h->device = dev;
   h->num_sms = prop.multiProcessorCount;
   h->log2_page = log2_page;
+  h->max_splits = d.dtype == FASTOCR_DTYPE_BF16 ? max_cluster_bf16(d.head_dim)
+                                                : max_cluster_f32(d.head_dim);
   h->ws_bytes = off;
   if (cudaMalloc(&h->ws, off) != cudaSuccess) {
     free(h);
     return FASTOCR_ERR_CUDA;
   }
   char* base = static_cast<char*>(h->ws);
-  h->part_ml = reinterpret_cast<float*>(base + o_ml);
-  h->part_acc = reinterpret_cast<float*>(base + o_acc);
   h->logits = reinterpret_cast<float*>(base + o_logits);
   h->sigma_part = reinterpret_cast<float*>(base + o_sigma);
-  h->cnt_head = reinterpret_cast<int32_t*>(base + o_cnt_head);
-  h->cnt_seq = reinterpret_cast<int32_t*>(base + o_cnt_seq);
   h->profile = reinterpret_cast<double*>(base + o_profile);
   h->status = reinterpret_cast<int32_t*>(base + o_status);
   if (cudaMemset(base + o_zero, 0, off - o_zero) != cudaSuccess ||
@@ -332,7 +325,7 @@ fastocr_status fastocr_device_status(fastocr_handle* h, int32_t* status, fastocr
 fastocr_status fastocr_set_splits(fastocr_handle* h, int32_t mode, int32_t splits) {
   if (!h) return FASTOCR_ERR_NULL;
   if (mode < 0 || mode > 2 || splits < 0) return FASTOCR_ERR_INVALID;
-  h->split_override[mode] = splits == 0 ? 0 : std::min(std::max(splits, 1), kMaxSplits);
+  h->split_override[mode] = splits == 0 ? 0 : std::min(std::max(splits, 1), h->max_splits);
   return FASTOCR_OK;
 }
 

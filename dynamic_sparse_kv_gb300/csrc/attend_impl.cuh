@@ -10,36 +10,59 @@ namespace fastocr {
 
 // ---------------------------------------------------------------- top-k
 
-// Sum the per-KV-head partial scores of sequence b into keys (shared memory),
+// Image scores and selection of sequence b, run by one CTA of NT threads:
+// sum the per-KV-head partial scores into keys (shared memory) in head order,
 // add the image mass to the profiler, and select the k largest keys (ties to
 // the lower offset) with a 4-pass 8-bit radix select over the fp32 bit
 // patterns (scores are >= 0, so the unsigned order is the float order). The
 // selection is written in ascending position order.
-static __device__ __noinline__ void score_and_select(const Params& p, int b, const AttendList& L,
-                                 unsigned char* smem) {
+template <int NT>
+__device__ __forceinline__ void score_and_select(const Params& p, int b, const AttendList& L,
+                                                 unsigned char* smem) {
+  constexpr int NW = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = L.n_img;
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
   int* hist = reinterpret_cast<int*>(smem + TopkSmem::hist_offset(p.max_img));
-  int* scratch = hist + 256;  // 64 ints
+  int* scratch = hist + 256;                                   // 2*NW + 2 ints
+  double* dscr = reinterpret_cast<double*>(scratch + 2 * NW + 2 + ((2 * NW + 2) & 1));
 
   double local = 0.0;
-  for (int i = tid; i < n; i += kThreads) {
-    float s = 0.f;
-    for (int hk = 0; hk < p.Hkv; ++hk)
-      s += __ldcg(p.sigma_part + ((size_t)b * p.Hkv + hk) * p.max_img + i);
-    keys[i] = __float_as_uint(s);
-    local += (double)s;
+  const float* sp_b = p.sigma_part + (size_t)b * p.Hkv * p.max_img;
+  for (int i0 = 0; i0 < n; i0 += 4 * NT) {
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int hk0 = 0; hk0 < p.Hkv; hk0 += 4) {   // 16 loads in flight, summed in head order
+      float v[4][4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * NT + tid;
+          v[c][u] = (hk0 + c < p.Hkv && i < n) ? __ldcg(sp_b + (size_t)(hk0 + c) * p.max_img + i) : 0.f;
+        }
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (hk0 + c < p.Hkv) s[u] += v[c][u];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * NT + tid;
+      if (i < n) {
+        keys[i] = __float_as_uint(s[u]);
+        local += (double)s[u];
+      }
+    }
   }
   if (p.profile_layer >= 0) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
-    double* dscr = reinterpret_cast<double*>(scratch + 32);
     if (lane == 0) dscr[warp] = local;
     __syncthreads();
     if (tid == 0) {
       double tot = 0.0;
-      for (int w = 0; w < kWarps; ++w) tot += dscr[w];
+      for (int w = 0; w < NW; ++w) tot += dscr[w];
       atomicAdd(p.profile + p.profile_layer, tot);
     }
   }
@@ -53,11 +76,15 @@ static __device__ __noinline__ void score_and_select(const Params& p, int b, con
   int krem = k;
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
+    for (int i = tid; i < 256; i += NT) hist[i] = 0;
     __syncthreads();
-    for (int i = tid; i < n; i += kThreads) {
-      const uint32_t key = keys[i];
-      if ((key & mask) == prefix) atomicAdd(hist + ((key >> shift) & 255u), 1);
+    for (int base = warp * 32; base < n; base += NT) {
+      const int i = base + lane;
+      const uint32_t key = i < n ? keys[i] : 0u;
+      const bool act = i < n && (key & mask) == prefix;
+      const uint32_t dig = act ? ((key >> shift) & 255u) : 256u;
+      const uint32_t same = __match_any_sync(0xffffffffu, dig);
+      if (act && lane == __ffs(same) - 1) atomicAdd(hist + dig, __popc(same));
     }
     __syncthreads();
     if (warp == 0) {
@@ -97,27 +124,27 @@ static __device__ __noinline__ void score_and_select(const Params& p, int b, con
   const uint32_t thr = prefix;  // the k-th largest key; krem of its copies are kept
 
   // --- stable compaction: warp w owns offsets [w*per, (w+1)*per), read 32 at a time
-  const int per = ((n + kWarps - 1) / kWarps + 31) / 32 * 32;
+  const int per = ((n + NW - 1) / NW + 31) / 32 * 32;
   const int lo = warp * per, hi = min(n, lo + per);
   const uint32_t lt_mask = (1u << lane) - 1u;
   int gt = 0, eq = 0;
   for (int base = lo; base < hi; base += 32) {
     const int i = base + lane;
-    const uint32_t key = i < hi ? keys[i] : 0u;
     const bool ok = i < hi;
+    const uint32_t key = ok ? keys[i] : 0u;
     gt += __popc(__ballot_sync(0xffffffffu, ok && key > thr));
     eq += __popc(__ballot_sync(0xffffffffu, ok && key == thr));
   }
   if (lane == 0) {
-    scratch[8 + warp] = gt;
-    scratch[16 + warp] = eq;
+    scratch[2 + warp] = gt;
+    scratch[2 + NW + warp] = eq;
   }
   __syncthreads();
   int eq_before = 0, out_before = 0;
   {
     int eb = 0;
-    for (int w = 0; w < kWarps; ++w) {
-      const int g_w = scratch[8 + w], e_w = scratch[16 + w];
+    for (int w = 0; w < NW; ++w) {
+      const int g_w = scratch[2 + w], e_w = scratch[2 + NW + w];
       int take = krem - eb;
       take = take < 0 ? 0 : (take > e_w ? e_w : take);
       if (w < warp) out_before += g_w + take;
@@ -142,6 +169,40 @@ static __device__ __noinline__ void score_and_select(const Params& p, int b, con
   }
 }
 
+constexpr int kSelectThreads = 1024;
+
+// Selection kernel of a focal layer: one CTA of 1024 threads per sequence,
+// launched right after the focal attend kernel (which left the per-KV-head
+// partial scores in the workspace).
+template <int NT>
+__global__ void __launch_bounds__(NT) select_kernel(const Params p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  int bad = 0;  // already reported by the attend kernel
+  const AttendList L = make_list<kFocal>(p, blockIdx.x, bad);
+  score_and_select<NT>(p, blockIdx.x, L, smem);
+}
+
+inline int select_smem_bytes(int max_img) {
+  return TopkSmem::hist_offset(max_img) + 256 * 4 + (2 * (kSelectThreads / 32) + 4) * 4 +
+         (kSelectThreads / 32) * 8 + 16;
+}
+
+inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, int smem, cudaStream_t stream,
+                                     cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
 // ---------------------------------------------------------------- main kernel
 
 template <typename T, int D, int MODE>
@@ -157,46 +218,108 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
 
   const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int bad = 0;
-  const AttendList L = make_list<MODE>(p, b, bad);
-
-  // this CTA's slice [r_lo, r_hi) of the attend list, in 16-token tiles
-  int chunk = (L.n_att + p.splits - 1) / p.splits;
-  chunk = (chunk + kTile - 1) / kTile * kTile;
-  const int r_lo = split * chunk;
-  const int r_hi = min(L.n_att, r_lo + chunk);
-  const int n_tiles = r_hi > r_lo ? (r_hi - r_lo + kTile - 1) / kTile : 0;
-  const int my_tiles = n_tiles > warp ? (n_tiles - warp + kWarps - 1) / kWarps : 0;
-
   const T* __restrict__ kg = static_cast<const T*>(p.k);
   const T* __restrict__ vg = static_cast<const T*>(p.v);
   const int32_t* __restrict__ bt = p.block_table + (size_t)b * p.max_pages;
   const int page_mask = (1 << p.log2_page) - 1;
-  unsigned char* pipe = smem + warp * kStages * SM::kStageBytes;
-  int* spos = reinterpret_cast<int*>(smem + SM::kPosOffset) + warp * kStages * kTile;
 
-  // Stage tile j of this warp: lanes 0..15 resolve the cache rows, then the
-  // warp copies 2 x 16 rows in 16-byte chunks (each instruction = whole rows).
-  auto issue = [&](int j) {
-    const int stage = j % kStages;
-    const int base = r_lo + (warp + j * kWarps) * kTile;
-    long long rowoff = -1;
-    if (lane < kTile) {
-      int pos = -1;
-      const int v = base + lane;
-      if (v < r_hi) {
-        pos = list_pos<MODE>(L, v, bad);
-        if (pos >= 0) {
-          const int page = __ldg(bt + (pos >> p.log2_page));
-          if (page < 0 || page >= p.num_pages) {
-            bad |= kDevBadPage;
-            pos = -1;
-          } else {
-            rowoff = ((((long long)page * p.Hkv + hkv) << p.log2_page) | (pos & page_mask)) * D;
-          }
+  // While the previous kernel on the stream may still run (programmatic
+  // dependent launch), warm L2 with this CTA's K/V rows, computed from a
+  // speculative read of the lengths, block table and selection. These reads
+  // only choose prefetch addresses (validated, never used for results), and
+  // every global read below bypasses L1, so stale values cannot leak in.
+  {
+    int ignore = 0;
+    const AttendList Ls = make_list<MODE>(p, b, ignore);
+    int ch = (Ls.n_att + p.splits - 1) / p.splits;
+    ch = (ch + kTile - 1) / kTile * kTile;
+    const int lo = split * ch, hi = min(Ls.n_att, lo + ch);
+    const uint32_t page_bytes = (uint32_t)(D * sizeof(T)) << p.log2_page;
+    auto prefetch_positions = [&](int pos_lo, int pos_hi) {
+      if (pos_hi <= pos_lo) return;
+      const int pg1 = (pos_hi - 1) >> p.log2_page;
+      for (int j = (pos_lo >> p.log2_page) + tid; j <= pg1; j += kThreads) {
+        const int page = __ldcg(bt + j);
+        if (page >= 0 && page < p.num_pages) {
+          const size_t off = ((size_t)page * p.Hkv + hkv) * ((size_t)D << p.log2_page);
+          prefetch_l2(kg + off, page_bytes);
+          prefetch_l2(vg + off, page_bytes);
         }
       }
-      spos[stage * kTile + lane] = pos;
+    };
+    prefetch_positions(lo, min(hi, Ls.n_pre));
+    const int sel_end = Ls.n_pre + Ls.n_sel;
+    if (MODE == kSparse) {
+      for (int v = max(lo, Ls.n_pre) + tid; v < min(hi, sel_end); v += kThreads) {
+        const int pos = __ldcg(Ls.sel + (v - Ls.n_pre));
+        if (pos < Ls.img_start || pos >= Ls.img_start + Ls.n_img) continue;
+        const int page = __ldcg(bt + (pos >> p.log2_page));
+        if (page < 0 || page >= p.num_pages) continue;
+        const size_t off =
+            ((((size_t)page * p.Hkv + hkv) << p.log2_page) | (size_t)(pos & page_mask)) * D;
+        prefetch_l2(kg + off, D * sizeof(T));
+        prefetch_l2(vg + off, D * sizeof(T));
+      }
+    }
+    const int t_lo = max(lo, sel_end), t_hi = hi;
+    if (t_hi > t_lo)
+      prefetch_positions(Ls.tail_start + (t_lo - sel_end), Ls.tail_start + (t_hi - sel_end));
+  }
+
+  // wait until the previous kernel on the stream has completed and its
+  // writes are visible (no-op when launched without the PDL attribute)
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  if (p.pdl_early) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  int bad = 0;
+  const AttendList L = make_list<MODE>(p, b, bad);
+
+  // this CTA's slice [r_lo, r_hi) of the attend list
+  int chunk = (L.n_att + p.splits - 1) / p.splits;
+  chunk = (chunk + kTile - 1) / kTile * kTile;
+  const int r_lo = split * chunk;
+  const int r_hi = min(L.n_att, r_lo + chunk);
+
+  unsigned char* pipe = smem + warp * kStages * SM::kStageBytes;
+  int* srow = reinterpret_cast<int*>(smem + SM::kRowOffset);
+
+  // Resolve list entries [rlo, rhi) (at most kSliceMax) to cache rows
+  // (page * H_kv + hkv) * page_size + slot, -1 if masked, into shared memory.
+  // All lookups of a thread are issued before any is used, so a round costs
+  // two memory latencies (selection, then block table) instead of two per tile.
+  auto resolve = [&](int rlo, int rhi) {
+    constexpr int kPer = kSliceMax / kThreads;
+    int pos[kPer], page[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int v = rlo + tid + j * kThreads;
+      pos[j] = v < rhi ? list_pos<MODE>(L, v, bad) : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) page[j] = pos[j] >= 0 ? __ldcg(bt + (pos[j] >> p.log2_page)) : -1;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int v = rlo + tid + j * kThreads;
+      if (v >= rhi) continue;
+      int row = -1;
+      if (pos[j] >= 0) {
+        if (page[j] < 0 || page[j] >= p.num_pages)
+          bad |= kDevBadPage;
+        else
+          row = ((page[j] * p.Hkv + hkv) << p.log2_page) | (pos[j] & page_mask);
+      }
+      srow[v - rlo] = row;
+    }
+  };
+
+  // Stage tile j (of this warp, within the current round) into its pipeline
+  // slot: 2 x 16 rows in 16-byte chunks, each instruction covering whole rows.
+  auto issue = [&](int j, int n_round) {
+    const int stage = j % kStages;
+    const int base = (warp + j * kWarps) * kTile;
+    long long rowoff = -1;
+    if (lane < kTile && base + lane < n_round) {
+      const int row = srow[base + lane];
+      rowoff = row >= 0 ? (long long)row * D : -1;
     }
     const uint32_t sb = smem_u32(pipe + stage * SM::kStageBytes);
 #pragma unroll
@@ -231,8 +354,8 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
     const T* qrow = static_cast<const T*>(p.q) + ((size_t)b * p.Hq + hkv * p.g + (have ? gid : 0)) * D;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-      sm_.qf[ks][0] = have ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * tig)) : 0u;
-      sm_.qf[ks][1] = have ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * tig)) : 0u;
+      sm_.qf[ks][0] = have ? __ldcg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * tig)) : 0u;
+      sm_.qf[ks][1] = have ? __ldcg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * tig)) : 0u;
     }
   } else {
     float* qs = reinterpret_cast<float*>(smem + SM::kQOffset);
@@ -250,20 +373,26 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
     __syncthreads();
   }
 
+  for (int rlo = r_lo; rlo < r_hi; rlo += kSliceMax) {
+  const int n_round = min(r_hi - rlo, kSliceMax);
+  resolve(rlo, rlo + n_round);
+  __syncthreads();
+  const int n_tiles = (n_round + kTile - 1) / kTile;
+  const int my_tiles = n_tiles > warp ? (n_tiles - warp + kWarps - 1) / kWarps : 0;
 #pragma unroll
   for (int j = 0; j < kStages - 1; ++j) {
-    if (j < my_tiles) issue(j);
+    if (j < my_tiles) issue(j, n_round);
     cp_async_commit();
   }
   for (int it = 0; it < my_tiles; ++it) {
-    if (it + kStages - 1 < my_tiles) issue(it + kStages - 1);
+    if (it + kStages - 1 < my_tiles) issue(it + kStages - 1, n_round);
     cp_async_commit();
     cp_async_wait<kStages - 1>();
     __syncwarp();
     const int stage = it % kStages;
     unsigned char* kS = pipe + stage * SM::kStageBytes;
     unsigned char* vS = kS + kTile * ROWB;
-    const int* tpos = spos + stage * kTile;
+    const int tbase = (warp + it * kWarps) * kTile;    // tile start within the round
 
     if constexpr (kMma) {
       // S^T[16 keys x 8 heads] = K[16 x D] . Q^T[D x 8]
@@ -277,7 +406,9 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
         ldmatrix_x4(a, kA + row * ROWB + ((ch ^ (row & 7)) << 4));
         mma_bf16(c, a, sm_.qf[ks][0], sm_.qf[ks][1]);
       }
-      const int posA = tpos[gid], posB = tpos[gid + 8];
+      // list position of tokens gid / gid+8 (= cache position in focal mode), -1 if masked
+      const int posA = (tbase + gid < n_round && srow[tbase + gid] >= 0) ? rlo + tbase + gid : -1;
+      const int posB = (tbase + gid + 8 < n_round && srow[tbase + gid + 8] >= 0) ? rlo + tbase + gid + 8 : -1;
       const float s0 = posA >= 0 ? c[0] * p.scale_log2 : kNegInf;
       const float s1 = posA >= 0 ? c[1] * p.scale_log2 : kNegInf;
       const float s2 = posB >= 0 ? c[2] * p.scale_log2 : kNegInf;
@@ -336,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
           s[h] = fmaf(kv.w, qv.w, s[h]);
         }
       }
-      const int pos = tpos[r];
+      const int pos = (tbase + r < n_round && srow[tbase + r] >= 0) ? rlo + tbase + r : -1;
 #pragma unroll
       for (int h = 0; h < kSlots; ++h) {
         s[h] += __shfl_xor_sync(0xffffffffu, s[h], 16);
@@ -384,6 +515,11 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
     __syncwarp();
   }
   cp_async_wait<0>();
+  __syncthreads();   // before the next round overwrites the row list
+  }
+  cp_async_wait<0>();
+  // the next kernel may now be scheduled; it waits for this grid to finish
+  if (!p.pdl_early) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   __syncthreads();
 
   // ---------------- CTA merge of the four warps -> split partial
@@ -422,148 +558,208 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
   }
   __syncthreads();
 
-  const size_t unit = (size_t)b * p.Hkv + hkv;
-  {
-    float* pacc = p.part_acc + ((unit * kMaxSplits + split) * kSlots) * D;
-    float* pml = p.part_ml + ((unit * kMaxSplits + split) * kSlots) * 2;
-    for (int e = tid; e < p.g * D; e += kThreads) {
-      const int h = e / D, d = e % D;
-      float M = kNegInf;
+  // ---------------- this CTA's partial (m, l, acc) of every head slot, in shared memory
+  float* cm = reinterpret_cast<float*>(smem + E::kPartM);
+  float* cl = reinterpret_cast<float*>(smem + E::kPartL);
+  float* cacc = reinterpret_cast<float*>(smem + E::kPartAcc);
+  for (int e = tid; e < kSlots * D; e += kThreads) {
+    const int h = e / D, d = e % D;
+    float M = kNegInf;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * kSlots + h]);
-      const float base = M == kNegInf ? 0.f : M;
-      float A = 0.f, Ls = 0.f;
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * kSlots + h]);
+    const float base = M == kNegInf ? 0.f : M;
+    float A = 0.f, Ls = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float sc = fast_exp2(wm[w * kSlots + h] - base);
-        A = fmaf(wacc[(w * kSlots + h) * D + d], sc, A);
-        Ls = fmaf(wl[w * kSlots + h], sc, Ls);
-      }
-      pacc[h * D + d] = A;
-      if (d == 0) {
-        pml[2 * h] = M;
-        pml[2 * h + 1] = Ls;
-      }
+    for (int w = 0; w < kWarps; ++w) {
+      const float sc = fast_exp2(wm[w * kSlots + h] - base);
+      A = fmaf(wacc[(w * kSlots + h) * D + d], sc, A);
+      Ls = fmaf(wl[w * kSlots + h], sc, Ls);
+    }
+    cacc[e] = A;
+    if (d == 0) {
+      cm[h] = M;
+      cl[h] = Ls;
     }
   }
   if (bad) atomicOr(p.status, bad);
-  __threadfence();
+  // The CTAs of one (sequence, KV head) form a thread-block cluster; the split
+  // partials are merged through distributed shared memory. Global writes of
+  // this CTA (focal logits) are fenced before the cluster barrier so that the
+  // other CTAs of the cluster read them after it.
+  if (MODE == kFocal) __threadfence();
   __syncthreads();
-  int* misc = reinterpret_cast<int*>(smem + E::kMisc);
-  if (tid == 0) misc[0] = atomicAdd(p.cnt_head + unit, 1) == p.splits - 1;
-  __syncthreads();
-  if (!misc[0]) return;
-  __threadfence();
-  if (tid == 0) p.cnt_head[unit] = 0;  // ready for the next launch
+  cluster_sync();
 
-  // ---------------- last CTA of (b, hkv): merge the splits
-  const int S = p.splits;
+  const int S = p.splits;               // == cluster size
+  const uint32_t rank = cluster_ctarank();
   float* sM = reinterpret_cast<float*>(smem + E::kM);
   float* sInvL = reinterpret_cast<float*>(smem + E::kInvL);
-  float* sScale = reinterpret_cast<float*>(smem + E::kScale);   // [S][8] then m,l staging
-  float* sml = wacc;                                             // [S][8][2] staging
-  const float* pml_u = p.part_ml + (unit * kMaxSplits) * kSlots * 2;
-  for (int e = tid; e < S * kSlots * 2; e += kThreads) sml[e] = __ldcg(pml_u + e);
+  float* sScale = reinterpret_cast<float*>(smem + E::kScale);  // [S][8]
+  float* rml = reinterpret_cast<float*>(smem + E::kRemoteMl);   // [S][8][2]
+  for (int e = tid; e < S * kSlots; e += kThreads) {
+    const int s = e / kSlots, h = e % kSlots;
+    rml[2 * e] = ld_dsmem_f32(cm + h, s);
+    rml[2 * e + 1] = ld_dsmem_f32(cl + h, s);
+  }
   __syncthreads();
-  for (int h = warp; h < p.g; h += kWarps) {
+  if (tid < kSlots) {
+    const int h = tid;
     float M = kNegInf;
-    for (int s = lane; s < S; s += 32) M = fmaxf(M, sml[(s * kSlots + h) * 2]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    for (int s = 0; s < S; ++s) M = fmaxf(M, rml[2 * (s * kSlots + h)]);
     const float base = M == kNegInf ? 0.f : M;
     float Ls = 0.f;
-    for (int s = lane; s < S; s += 32)
-      Ls += sml[(s * kSlots + h) * 2 + 1] * fast_exp2(sml[(s * kSlots + h) * 2] - base);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
-    if (lane == 0) {
-      sM[h] = base;
-      sInvL[h] = Ls > 0.f ? __frcp_rn(Ls) : 0.f;
-    }
+    for (int s = 0; s < S; ++s)
+      Ls = fmaf(rml[2 * (s * kSlots + h) + 1], fast_exp2(rml[2 * (s * kSlots + h)] - base), Ls);
+    sM[h] = base;
+    sInvL[h] = Ls > 0.f ? __frcp_rn(Ls) : 0.f;
   }
   __syncthreads();
   for (int e = tid; e < S * kSlots; e += kThreads) {
-    const int s = e / kSlots, h = e % kSlots;
-    sScale[e] = h < p.g ? fast_exp2(sml[e * 2] - sM[h]) * sInvL[h] : 0.f;
+    const int h = e % kSlots;
+    sScale[e] = fast_exp2(rml[2 * e] - sM[h]) * sInvL[h];
   }
   __syncthreads();
+
+  // ---------------- outputs: CTA `rank` owns a slice of the (head, 4-dim) pairs
   {
-    const float* pacc_u = p.part_acc + (unit * kMaxSplits) * kSlots * D;
+    constexpr int C4 = D / 4;
+    const int n_pairs = p.g * C4;
+    const int per = (n_pairs + S - 1) / S;
+    const int e_hi = min(n_pairs, (int)(rank + 1) * per);
     T* outp = static_cast<T*>(p.out) + ((size_t)b * p.Hq + (size_t)hkv * p.g) * D;
-    for (int e = tid; e < p.g * D; e += kThreads) {
-      const int h = e / D, d = e % D;
-      float A0 = 0.f, A1 = 0.f, A2 = 0.f, A3 = 0.f;
-      int s = 0;
-      for (; s + 4 <= S; s += 4) {
-        A0 = fmaf(__ldcg(pacc_u + ((size_t)(s + 0) * kSlots + h) * D + d), sScale[(s + 0) * kSlots + h], A0);
-        A1 = fmaf(__ldcg(pacc_u + ((size_t)(s + 1) * kSlots + h) * D + d), sScale[(s + 1) * kSlots + h], A1);
-        A2 = fmaf(__ldcg(pacc_u + ((size_t)(s + 2) * kSlots + h) * D + d), sScale[(s + 2) * kSlots + h], A2);
-        A3 = fmaf(__ldcg(pacc_u + ((size_t)(s + 3) * kSlots + h) * D + d), sScale[(s + 3) * kSlots + h], A3);
+    for (int e = (int)rank * per + tid; e < e_hi; e += kThreads) {
+      const int h = e / C4, c4 = e % C4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s0 = 0; s0 < S; s0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          v[u] = s0 + u < S ? ld_dsmem_f32x4(cacc + h * D + 4 * c4, s0 + u)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float sc = s0 + u < S ? sScale[(s0 + u) * kSlots + h] : 0.f;
+          acc.x = fmaf(v[u].x, sc, acc.x);
+          acc.y = fmaf(v[u].y, sc, acc.y);
+          acc.z = fmaf(v[u].z, sc, acc.z);
+          acc.w = fmaf(v[u].w, sc, acc.w);
+        }
       }
-      for (; s < S; ++s)
-        A0 = fmaf(__ldcg(pacc_u + ((size_t)s * kSlots + h) * D + d), sScale[s * kSlots + h], A0);
-      const float o = (A0 + A1) + (A2 + A3);
-      if constexpr (kMma)
-        outp[h * D + d] = __float2bfloat16_rn(o);
-      else
-        outp[h * D + d] = o;
+      T* o = outp + h * D + 4 * c4;
+      if constexpr (kMma) {
+        uint2 w;
+        w.x = pack_bf16(acc.x, acc.y);
+        w.y = pack_bf16(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(o) = w;
+      } else {
+        *reinterpret_cast<float4*>(o) = acc;
+      }
     }
   }
-  if constexpr (MODE == kFocal) {
 
-    // ---------------- focal: this group's share of the image scores
-    {
-      float Mh[kSlots], iL[kSlots];
+  // ---------------- focal: this group's share of the image scores, split over the cluster
+  if constexpr (MODE == kFocal) {
+    float Mh[kSlots], iL[kSlots];
 #pragma unroll
-      for (int h = 0; h < kSlots; ++h) {
-        Mh[h] = h < p.g ? sM[h] : 0.f;
-        iL[h] = h < p.g ? sInvL[h] : 0.f;
+    for (int h = 0; h < kSlots; ++h) {
+      Mh[h] = h < p.g ? sM[h] : 0.f;
+      iL[h] = h < p.g ? sInvL[h] : 0.f;
+    }
+    const size_t unit = (size_t)b * p.Hkv + hkv;
+    float* sp = p.sigma_part + unit * p.max_img;
+    const int nper = (L.n_img + S - 1) / S;
+    const int i_lo = (int)rank * nper, i_hi = min(L.n_img, i_lo + nper);
+    for (int i0 = i_lo; i0 < i_hi; i0 += 4 * kThreads) {
+      float4 x[4][2];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * kThreads + tid;
+        const float4* src4 = reinterpret_cast<const float4*>(logit_base + (size_t)i * kSlots);
+        x[u][0] = i < i_hi ? __ldcg(src4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[u][1] = i < i_hi ? __ldcg(src4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      float* sp = p.sigma_part + unit * p.max_img;
-      for (int i = tid; i < L.n_img; i += kThreads) {
-        const float4 x0 = __ldcg(reinterpret_cast<const float4*>(logit_base + (size_t)i * kSlots));
-        const float4 x1 = __ldcg(reinterpret_cast<const float4*>(logit_base + (size_t)i * kSlots + 4));
-        const float x[kSlots] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * kThreads + tid;
+        const float xv[kSlots] = {x[u][0].x, x[u][0].y, x[u][0].z, x[u][0].w,
+                                  x[u][1].x, x[u][1].y, x[u][1].z, x[u][1].w};
         float sg = 0.f;
 #pragma unroll
         for (int h = 0; h < kSlots; ++h)
-          if (h < p.g) sg = fmaf(fast_exp2(x[h] - Mh[h]), iL[h], sg);
-        sp[i] = sg;
+          if (h < p.g) sg = fmaf(fast_exp2(xv[h] - Mh[h]), iL[h], sg);
+        if (i < i_hi) sp[i] = sg;
       }
     }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) misc[1] = atomicAdd(p.cnt_seq + b, 1) == p.Hkv - 1;
-    __syncthreads();
-    if (!misc[1]) return;
-    __threadfence();
-    if (tid == 0) p.cnt_seq[b] = 0;
-    score_and_select(p, b, L, smem);
   }
+  // no CTA may leave while another still reads its shared memory
+  cluster_sync();
 }
 
+// Launch with programmatic dependent launch: the grid may be scheduled while
+// the previous kernel on the stream finishes its epilogue; it waits for that
+// kernel's completion (griddepcontrol.wait) before reading any global memory.
+// A focal layer is two launches: the attend kernel, then the selection kernel.
 template <typename T, int D, int MODE>
 cudaError_t launch_attend(const Params& p, cudaStream_t stream) {
-  const int smem = attend_smem_bytes<T, D>(MODE == kFocal ? p.max_img : 0);
-  dim3 grid(p.splits, p.Hkv, p.B);
-  attend_kernel<T, D, MODE><<<grid, kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(p.splits, p.Hkv, p.B), dim3(kThreads, 1, 1),
+                                      attend_smem_bytes<T, D>(), stream, attr);
+  attr[1].id = cudaLaunchAttributeClusterDimension;   // the splits of one (b, hkv)
+  attr[1].val.clusterDim.x = p.splits;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attend_kernel<T, D, MODE>, p);
+  if (e != cudaSuccess || MODE != kFocal) return e;
+  cudaLaunchAttribute attr2[1];
+  cudaLaunchConfig_t cfg2 = pdl_config(dim3(p.B, 1, 1), dim3(kSelectThreads, 1, 1),
+                                       select_smem_bytes(p.max_img), stream, attr2);
+  return cudaLaunchKernelEx(&cfg2, select_kernel<kSelectThreads>, p);
 }
 
-// Raise the dynamic shared-memory limit of every mode of one (T, D) once per
-// device, before any launch (so never inside a stream capture).
+// Raise the dynamic shared-memory limits once per device, before any launch
+// (so never inside a stream capture).
+template <typename Kern>
+cudaError_t prepare_attend(Kern k, int bytes) {
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
+
 template <typename T, int D>
 cudaError_t prepare_all_modes() {
-  const int bytes = attend_smem_bytes<T, D>(kMaxImg);
+  const int bytes = attend_smem_bytes<T, D>();
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(attend_kernel<T, D, kFull>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
-  if ((e = cudaFuncSetAttribute(attend_kernel<T, D, kFocal>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
-  if ((e = cudaFuncSetAttribute(attend_kernel<T, D, kSparse>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
-  return cudaFuncSetAttribute(attend_kernel<T, D, kRswa>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if ((e = prepare_attend(attend_kernel<T, D, kFull>, bytes))) return e;
+  if ((e = prepare_attend(attend_kernel<T, D, kFocal>, bytes))) return e;
+  if ((e = prepare_attend(attend_kernel<T, D, kSparse>, bytes))) return e;
+  if ((e = prepare_attend(attend_kernel<T, D, kRswa>, bytes))) return e;
+  return cudaFuncSetAttribute(select_kernel<kSelectThreads>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              select_smem_bytes(kMaxImg));
+}
+
+// Largest cluster (<= kMaxSplits) of this kernel that the device can co-schedule.
+template <typename T, int D>
+int max_cluster_size() {
+  for (int c = kMaxSplits; c > 1; c >>= 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(c, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = attend_smem_bytes<T, D>();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = c;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, attend_kernel<T, D, kFull>, &cfg) == cudaSuccess && n > 0)
+      return c;
+    cudaGetLastError();
+  }
+  return 1;
 }
 
 template <typename T, int D>

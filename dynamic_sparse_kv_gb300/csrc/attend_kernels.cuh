@@ -36,7 +36,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 16;      // tokens per warp tile
 constexpr int kSlots = 8;      // query-head slots per KV head (g <= 8)
 constexpr int kStages = 3;     // cp.async pipeline depth per warp
-constexpr int kMaxSplits = 64;
+constexpr int kMaxSplits = 16;  // = the largest thread-block cluster used
 constexpr int kMaxImg = 16384; // image tokens whose scores fit in shared memory
 
 enum Mode : int { kFull = 0, kFocal = 1, kSparse = 2, kRswa = 3 };
@@ -68,14 +68,11 @@ struct Params {
   int splits;
   float scale_log2;          // log2(e) / sqrt(d)
   // workspace
-  float* part_ml;            // [B, H_kv, kMaxSplits, kSlots, 2]
-  float* part_acc;           // [B, H_kv, kMaxSplits, kSlots, D]
   float* logits;             // [B, H_kv, max_img, kSlots]
   float* sigma_part;         // [B, H_kv, max_img]
-  int32_t* cnt_head;         // [B * H_kv]
-  int32_t* cnt_seq;          // [B]
   double* profile;           // [num_layers]
   int profile_layer;
+  int pdl_early;             // grid fits on the SMs next to the next one: trigger it at once
   int32_t* status;
   int max_img;
 };
@@ -123,6 +120,38 @@ __device__ __forceinline__ void mma_bf16(float c[4], const uint32_t a[4], uint32
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// Thread-block cluster: barrier (release/acquire) and distributed shared memory.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+// Load from the same shared-memory offset as `local` in CTA `rank` of the cluster.
+__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_dsmem_f32x4(const float* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(remote)
+               : "memory");
+  return v;
+}
+// Bring `bytes` (multiple of 16) at `p` into L2; never faults on a valid address.
+__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(ptr), "r"(bytes) : "memory");
+}
 // 2^x on the special-function unit (x = -inf gives +0).
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -166,7 +195,7 @@ template <int MODE>
 __device__ __forceinline__ AttendList make_list(const Params& p, int b, int& bad) {
   AttendList L;
   const int cap = p.max_pages << p.log2_page;
-  int n_t = __ldg(p.seq_len + b);
+  int n_t = __ldcg(p.seq_len + b);
   if (n_t < 1 || n_t > cap) {
     bad |= kDevBadSeqLen;
     n_t = n_t < 0 ? 0 : (n_t > cap ? cap : n_t);
@@ -178,7 +207,7 @@ __device__ __forceinline__ AttendList make_list(const Params& p, int b, int& bad
   L.img_start = 0;
   L.n_img = 0;
   if (MODE == kFocal || MODE == kSparse) {
-    int s = __ldg(p.img_range + 2 * b), n = __ldg(p.img_range + 2 * b + 1);
+    int s = __ldcg(p.img_range + 2 * b), n = __ldcg(p.img_range + 2 * b + 1);
     if (s < 0 || n < 0 || s > n_t || n > n_t - s || (MODE == kFocal && n > p.max_img)) {
       bad |= kDevBadImg;
       s = s < 0 ? 0 : (s > n_t ? n_t : s);
@@ -192,7 +221,7 @@ __device__ __forceinline__ AttendList make_list(const Params& p, int b, int& bad
     L.n_pre = n_t;
     L.n_att = n_t;
   } else if (MODE == kSparse) {
-    int k = __ldg(p.k_in + b);
+    int k = __ldcg(p.k_in + b);
     const int k_cap = L.n_img < p.idx_stride ? L.n_img : p.idx_stride;
     if (k < 0 || k > k_cap) {
       bad |= kDevBadSelection;
@@ -220,7 +249,7 @@ __device__ __forceinline__ int list_pos(const AttendList& L, int v, int& bad) {
   v -= L.n_pre;
   if (MODE == kSparse) {
     if (v < L.n_sel) {
-      int pos = __ldg(L.sel + v);
+      int pos = __ldcg(L.sel + v);
       if (pos < L.img_start || pos >= L.img_start + L.n_img) {
         bad |= kDevBadSelection;
         return -1;
@@ -234,44 +263,47 @@ __device__ __forceinline__ int list_pos(const AttendList& L, int v, int& bad) {
 
 // ---------------------------------------------------------------- shared memory
 
+constexpr int kSliceMax = 2048;  // attend-list entries resolved to cache rows per round
+
 template <typename T, int D>
 struct Smem {
   static constexpr int kRowBytes = D * (int)sizeof(T);
   static constexpr int kStageBytes = 2 * kTile * kRowBytes;          // K rows then V rows
   static constexpr int kPipeBytes = kWarps * kStages * kStageBytes;
-  static constexpr int kPosOffset = kPipeBytes;                      // int pos[W][S][16]
-  static constexpr int kQOffset = kPosOffset + kWarps * kStages * kTile * 4;  // f32 q[8][D]
-  static constexpr int kMainBytes = kQOffset + kSlots * D * 4;
+  static constexpr int kRowOffset = kPipeBytes;                      // int row[kSliceMax]
+  static constexpr int kQOffset = kRowOffset + kSliceMax * 4;        // f32 path: q[8][D]
+  static constexpr int kMainBytes = kQOffset + (sizeof(T) == 4 ? kSlots * D * 4 : 0);
 };
 
 template <int D>
 struct EpiSmem {
-  // wm[W][8], wl[W][8], wacc[W][8][D], then the merge area: M[8], invL[8],
-  // scale[kMaxSplits][8], misc ints
+  // per-warp partials wm[W][8], wl[W][8], wacc[W][8][D]; the CTA partial
+  // (read by the other CTAs of the cluster) m[8], l[8], acc[8][D]; merge
+  // scratch M[8], invL[8], scale[kMaxSplits][8], remote (m,l)[kMaxSplits][8][2]
   static constexpr int kWm = 0;
   static constexpr int kWl = kWm + kWarps * kSlots * 4;
   static constexpr int kWacc = kWl + kWarps * kSlots * 4;
-  static constexpr int kM = kWacc + kWarps * kSlots * D * 4;
+  static constexpr int kPartM = kWacc + kWarps * kSlots * D * 4;
+  static constexpr int kPartL = kPartM + kSlots * 4;
+  static constexpr int kPartAcc = kPartL + kSlots * 4;
+  static constexpr int kM = kPartAcc + kSlots * D * 4;
   static constexpr int kInvL = kM + kSlots * 4;
   static constexpr int kScale = kInvL + kSlots * 4;
-  static constexpr int kMisc = kScale + kMaxSplits * kSlots * 4;
-  static constexpr int kBytes = kMisc + 64;
+  static constexpr int kRemoteMl = kScale + kMaxSplits * kSlots * 4;
+  static constexpr int kBytes = kRemoteMl + kMaxSplits * kSlots * 2 * 4;
 };
 
 struct TopkSmem {
-  // keys[max_img] (uint32), then hist[256] at a 16-byte boundary, then 64
-  // ints of scan scratch (the upper half also holds kWarps doubles)
+  // keys[max_img] (uint32), then hist[256] at a 16-byte boundary, then scan
+  // scratch (sized by the selection kernel)
   __host__ __device__ static int hist_offset(int max_img) { return (max_img * 4 + 15) / 16 * 16; }
-  __host__ __device__ static int bytes(int max_img) { return hist_offset(max_img) + 256 * 4 + 64 * 4; }
 };
 
 template <typename T, int D>
-inline int attend_smem_bytes(int max_img) {
+inline int attend_smem_bytes() {
   int a = Smem<T, D>::kMainBytes;
   int b = EpiSmem<D>::kBytes;
-  int c = TopkSmem::bytes(max_img);
-  int m = a > b ? a : b;
-  return m > c ? m : c;
+  return a > b ? a : b;
 }
 
 // ---------------------------------------------------------------- warp reductions

@@ -11,14 +11,13 @@ cudaError_t launch_bf16(int head_dim, int mode, const Params& p, cudaStream_t s)
   return cudaErrorInvalidValue;
 }
 
-int smem_bytes_bf16(int head_dim, int max_img) {
-  return head_dim == 64 ? attend_smem_bytes<__nv_bfloat16, 64>(max_img)
-                        : attend_smem_bytes<__nv_bfloat16, 128>(max_img);
-}
-
 cudaError_t prepare_bf16() {
   cudaError_t e = prepare_all_modes<__nv_bfloat16, 64>();
   return e != cudaSuccess ? e : prepare_all_modes<__nv_bfloat16, 128>();
+}
+
+int max_cluster_bf16(int head_dim) {
+  return head_dim == 64 ? max_cluster_size<__nv_bfloat16, 64>() : max_cluster_size<__nv_bfloat16, 128>();
 }
 
 }  // namespace fastocr

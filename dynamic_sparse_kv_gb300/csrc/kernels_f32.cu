@@ -11,14 +11,13 @@ cudaError_t launch_f32(int head_dim, int mode, const Params& p, cudaStream_t s) 
   return cudaErrorInvalidValue;
 }
 
-int smem_bytes_f32(int head_dim, int max_img) {
-  return head_dim == 64 ? attend_smem_bytes<float, 64>(max_img)
-                        : attend_smem_bytes<float, 128>(max_img);
-}
-
 cudaError_t prepare_f32() {
   cudaError_t e = prepare_all_modes<float, 64>();
   return e != cudaSuccess ? e : prepare_all_modes<float, 128>();
+}
+
+int max_cluster_f32(int head_dim) {
+  return head_dim == 64 ? max_cluster_size<float, 64>() : max_cluster_size<float, 128>();
 }
 
 }  // namespace fastocr

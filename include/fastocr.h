@@ -134,7 +134,9 @@ fastocr_status fastocr_full_attend(fastocr_handle* h, const void* q, const fasto
  * k_b = ceil(tau*N_img_b) image tokens of every sequence, written to
  * idx[b*idx_stride + 0 .. k_b-1] as ascending absolute positions, with k_b in
  * k_out[b]. Scoring and selection run on the device (no host round trip).
- * tau in (0, 1]; idx_stride >= ceil(tau*max_img_tokens).
+ * tau in (0, 1]; idx_stride >= ceil(tau*max_img_tokens). Two kernels run
+ * back to back on `stream`: the attention (which also leaves each KV head's
+ * share of the image scores in the workspace) and the selection.
  * profile_layer >= 0 (< num_layers) adds the image probability mass summed
  * over sequences and query heads to that layer's profiler slot (warm-up);
  * -1 disables profiling. */
@@ -147,7 +149,9 @@ fastocr_status fastocr_focal_attend(fastocr_handle* h, const void* q, const fast
  * the k[b] selected image positions idx[b*idx_stride + 0 .. k[b]-1] (any
  * order, each inside the image range), and the generated tokens
  * [start + N_img, N_t). Passing F_last (the previous step's selection of the
- * deepest focal layer) here is Cross-Step Fixation Reuse. */
+ * deepest focal layer) here is Cross-Step Fixation Reuse. A k[b] outside
+ * [0, min(N_img, idx_stride)] or a position outside the image range is
+ * reported as FASTOCR_DEV_BAD_SELECTION and clamped / masked. */
 fastocr_status fastocr_sparse_attend(fastocr_handle* h, const void* q, const fastocr_kv* kv,
                                      const int32_t* img_range, const int32_t* idx,
                                      int32_t idx_stride, const int32_t* k, void* out,
@@ -177,7 +181,8 @@ fastocr_status fastocr_device_status(fastocr_handle* h, int32_t* status, fastocr
 
 /* Override the split-K factor of a mode (0 = full/focal, 1 = sparse,
  * 2 = R-SWA); 0 restores the automatic choice. Splits are clamped to
- * [1, 64]. */
+ * [1, 16] (the splits of one sequence and KV head form one thread-block
+ * cluster) and to the largest cluster the device co-schedules. */
 fastocr_status fastocr_set_splits(fastocr_handle* h, int32_t mode, int32_t splits);
 
 #ifdef __cplusplus

@@ -24,19 +24,28 @@ def np64(t: torch.Tensor) -> np.ndarray:
 
 
 class KVCache:
-    """Logical fp64 copies of (layer, sequence) caches for the oracle, cached."""
+    """Logical fp64 copies of (layer, sequence) caches for the oracle, kept in a
+    small LRU (a byte budget) so full-size workloads fit in host memory."""
 
-    def __init__(self, case):
+    def __init__(self, case, budget_bytes=3 << 30):
         self.case = case
         self.n_max = case.wl.max_tokens
+        self.budget = budget_bytes
         self._memo = {}
 
     def __call__(self, layer: int, b: int):
         key = (layer, b)
-        if key not in self._memo:
-            K, V = self.case.logical_kv(layer, b, self.n_max)
-            self._memo[key] = (np64(K), np64(V))
-        return self._memo[key]
+        if key in self._memo:
+            val = self._memo.pop(key)
+            self._memo[key] = val
+            return val
+        K, V = self.case.logical_kv(layer, b, self.n_max)
+        val = (np64(K), np64(V))
+        self._memo[key] = val
+        while len(self._memo) > 1 and sum(k.nbytes + v.nbytes for k, v in self._memo.values()) \
+                > self.budget:
+            self._memo.pop(next(iter(self._memo)))
+        return val
 
 
 def check_selection(gpu, oracle_sel, sigma, img_start, where=""):
