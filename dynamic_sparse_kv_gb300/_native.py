@@ -69,6 +69,9 @@ def _load() -> ctypes.CDLL:
         "fastocr_profiler_select": ([P, I32, ctypes.POINTER(I32), ctypes.POINTER(F64), P], I32),
         "fastocr_device_status": ([P, ctypes.POINTER(I32), P], I32),
         "fastocr_set_splits": ([P, I32, I32], I32),
+        "fastocr_focal_attend_noalloc": ([ctypes.POINTER(fastocr_dims), P,
+                                          ctypes.POINTER(fastocr_kv), P, F64, P, P, I32, P, P, P],
+                                         I32),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -176,3 +179,17 @@ def fastocr_device_status(handle, stream=None) -> int:
 
 def fastocr_set_splits(handle, mode, splits) -> None:
     _check("fastocr_set_splits", lib.fastocr_set_splits(handle, int(mode), int(splits)))
+
+
+NOALLOC_MAX_UNITS_IMG = 65536   # FASTOCR_NOALLOC_MAX_UNITS_IMG
+
+
+def fastocr_focal_attend_noalloc(dims: fastocr_dims, q, kv: fastocr_kv, img_range, tau, out, idx,
+                                 idx_stride, k_out, status, stream=None) -> None:
+    """Focal layer without a handle, for callers that may not allocate GPU
+    memory where they run; its scratch is a fixed array inside the library."""
+    _check("fastocr_focal_attend_noalloc",
+           lib.fastocr_focal_attend_noalloc(ctypes.byref(dims), _ptr(q), ctypes.byref(kv),
+                                            _ptr(img_range), float(tau), _ptr(out), _ptr(idx),
+                                            int(idx_stride), _ptr(k_out), _ptr(status),
+                                            _stream(stream)))

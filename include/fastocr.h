@@ -185,6 +185,41 @@ fastocr_status fastocr_device_status(fastocr_handle* h, int32_t* status, fastocr
  * cluster) and to the largest cluster the device co-schedules. */
 fastocr_status fastocr_set_splits(fastocr_handle* h, int32_t mode, int32_t splits);
 
+/* Allocation-free focal layer. The pages describe no such call; it exists
+ * for callers that may not allocate GPU memory at the point where they run
+ * attention -- for example code living inside another framework's memory
+ * pool, plugins whose host forbids cudaMalloc once started, or latency-
+ * critical loops that must not take the driver's allocation locks. It needs
+ * no handle: it computes exactly what fastocr_focal_attend computes (same
+ * kernels, same split rule, profiling off) but keeps its scratch -- the image
+ * logits and per-KV-head scores -- in one fixed array of
+ * FASTOCR_NOALLOC_MAX_UNITS_IMG * 9 floats (about 2.4 MB) compiled into the
+ * library, which every GPU that loads the library holds until the process
+ * exits. It calls no cudaMalloc or cudaFree and no allocating library
+ * routine.
+ *
+ * dims: shapes as for fastocr_create (num_layers is ignored); the problem
+ * must satisfy batch * num_kv_heads * max_img_tokens <=
+ * FASTOCR_NOALLOC_MAX_UNITS_IMG, otherwise the call returns
+ * FASTOCR_ERR_UNSUPPORTED without launching anything. q, kv, img_range, tau,
+ * out, idx, idx_stride, k_out: as for fastocr_focal_attend. status: device
+ * int32 the kernels OR FASTOCR_DEV_* bits into (the caller clears it).
+ *
+ * The first call on a device sets that device up (looks up the device
+ * address of the fixed array with cudaGetSymbolAddress, raises the kernels'
+ * shared-memory limits, reads the SM count); make that first call outside
+ * any stream capture. Every call on a device uses the same array and leaves
+ * its contents behind; nothing in it needs clearing because each call writes
+ * every value it later reads. Calls whose executions overlap on the GPU
+ * (different streams, or several host threads) race on the array: order
+ * them. */
+#define FASTOCR_NOALLOC_MAX_UNITS_IMG 65536
+fastocr_status fastocr_focal_attend_noalloc(const fastocr_dims* dims, const void* q,
+                                            const fastocr_kv* kv, const int32_t* img_range,
+                                            double tau, void* out, int32_t* idx,
+                                            int32_t idx_stride, int32_t* k_out, int32_t* status,
+                                            fastocr_stream stream);
+
 #ifdef __cplusplus
 }
 #endif
