@@ -44,6 +44,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="qwen7b_b1")
     ap.add_argument("--tau", type=float, default=None)
+    ap.add_argument("--set", action="append", default=[], metavar="FIELD=VALUE",
+                    help="override a workload field, e.g. --set batch=8 (profiling runs)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -261,6 +263,9 @@ def run_gpu(args, rank, world, local_rank):
     wl = synth.workload(args.workload)
     if args.tau is not None:
         wl = wl.with_(tau=args.tau)
+    for item in args.set:
+        key, val = item.split("=", 1)
+        wl = wl.with_(**{key: type(getattr(wl, key))(val)})
     wl = wl.with_(seed=wl.seed + 1000 * rank)
     K, W = args.steps, args.warmup
     assert W >= 3, "at least 3 warm-up steps"

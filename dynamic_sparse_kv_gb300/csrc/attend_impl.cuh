@@ -12,25 +12,28 @@ namespace fastocr {
 
 // Image scores and selection of sequence b, run by one CTA of NT threads:
 // sum the per-KV-head partial scores into keys (shared memory) in head order,
-// add the image mass to the profiler, and select the k largest keys (ties to
-// the lower offset) with a 4-pass 8-bit radix select over the fp32 bit
-// patterns (scores are >= 0, so the unsigned order is the float order). The
-// selection is written in ascending position order.
+// add the image mass to the profiler (warm-up only), and select the k largest
+// keys (ties to the lower offset) with an 8-bit radix select over the fp32
+// bit patterns (scores are >= 0, so the unsigned order is the float order).
+// The selection is written in ascending position order.
 template <int NT>
 __device__ __forceinline__ void score_and_select(const Params& p, int b, const AttendList& L,
                                                  unsigned char* smem) {
   constexpr int NW = NT / 32;
+  constexpr int kSub = 4;                                       // sub-histograms
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = L.n_img;
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
-  int* hist = reinterpret_cast<int*>(smem + TopkSmem::hist_offset(p.max_img));
-  int* scratch = hist + 256;                                   // 2*NW + 2 ints
-  double* dscr = reinterpret_cast<double*>(scratch + 2 * NW + 2 + ((2 * NW + 2) & 1));
+  int* hist = reinterpret_cast<int*>(smem + TopkSmem::hist_offset(p.max_img));   // [256]
+  int* sub = hist + 256;                                        // [kSub][256]
+  int* scratch = sub + kSub * 256;                              // [4 + 2*NW]
+  double* dscr = reinterpret_cast<double*>(scratch + 4 + 2 * NW);  // [NW]
 
+  const bool profiling = p.profile_layer >= 0;
   double local = 0.0;
   const float* sp_b = p.sigma_part + (size_t)b * p.Hkv * p.max_img;
   for (int i0 = 0; i0 < n; i0 += 4 * NT) {
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    float sv[4] = {0.f, 0.f, 0.f, 0.f};
     for (int hk0 = 0; hk0 < p.Hkv; hk0 += 4) {   // 16 loads in flight, summed in head order
       float v[4][4];
 #pragma unroll
@@ -44,47 +47,59 @@ __device__ __forceinline__ void score_and_select(const Params& p, int b, const A
       for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          if (hk0 + c < p.Hkv) s[u] += v[c][u];
+          if (hk0 + c < p.Hkv) sv[u] += v[c][u];
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + u * NT + tid;
       if (i < n) {
-        keys[i] = __float_as_uint(s[u]);
-        local += (double)s[u];
+        keys[i] = __float_as_uint(sv[u]);
+        if (profiling) local += (double)sv[u];
       }
     }
   }
-  if (p.profile_layer >= 0) {
+  if (profiling) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
     if (lane == 0) dscr[warp] = local;
-    __syncthreads();
-    if (tid == 0) {
-      double tot = 0.0;
-      for (int w = 0; w < NW; ++w) tot += dscr[w];
-      atomicAdd(p.profile + p.profile_layer, tot);
-    }
   }
-  const int k = keep_count(p.tau, n);
-  if (tid == 0) p.k_out[b] = k;
+  if (tid == 0) {
+    const int k = keep_count(p.tau, n);   // double arithmetic: one thread only
+    scratch[2] = k;
+    p.k_out[b] = k;
+  }
   __syncthreads();
+  if (profiling && tid == 0) {
+    double tot = 0.0;
+    for (int w = 0; w < NW; ++w) tot += dscr[w];
+    atomicAdd(p.profile + p.profile_layer, tot);
+  }
+  const int k = scratch[2];
   if (k == 0) return;
 
-  // --- radix select of the k-th largest key
+  // --- radix select: find the k-th largest key, or stop early once every key
+  // sharing the decided prefix is to be kept
   uint32_t prefix = 0, mask = 0;
   int krem = k;
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 256; i += NT) hist[i] = 0;
+    for (int i = tid; i < kSub * 256; i += NT) sub[i] = 0;
     __syncthreads();
+    int* my = sub + (warp & (kSub - 1)) * 256;
     for (int base = warp * 32; base < n; base += NT) {
       const int i = base + lane;
       const uint32_t key = i < n ? keys[i] : 0u;
       const bool act = i < n && (key & mask) == prefix;
       const uint32_t dig = act ? ((key >> shift) & 255u) : 256u;
       const uint32_t same = __match_any_sync(0xffffffffu, dig);
-      if (act && lane == __ffs(same) - 1) atomicAdd(hist + dig, __popc(same));
+      if (act && lane == __ffs(same) - 1) atomicAdd(my + dig, __popc(same));
+    }
+    __syncthreads();
+    for (int i = tid; i < 256; i += NT) {
+      int t = 0;
+#pragma unroll
+      for (int j = 0; j < kSub; ++j) t += sub[j * 256 + i];
+      hist[i] = t;
     }
     __syncthreads();
     if (warp == 0) {
@@ -109,6 +124,7 @@ __device__ __forceinline__ void score_and_select(const Params& p, int b, const A
           if (c + cnt[j] >= krem) {
             scratch[0] = 255 - 8 * lane - j;
             scratch[1] = c;
+            scratch[3] = cnt[j];
             break;
           }
           c += cnt[j];
@@ -119,9 +135,10 @@ __device__ __forceinline__ void score_and_select(const Params& p, int b, const A
     prefix |= (uint32_t)scratch[0] << shift;
     mask |= 255u << shift;
     krem -= scratch[1];
-    __syncthreads();
+    if (krem == scratch[3]) break;   // all keys with this prefix are kept
   }
-  const uint32_t thr = prefix;  // the k-th largest key; krem of its copies are kept
+  // keep: (key & mask) > prefix, or == prefix for the first krem such keys
+  const uint32_t thr = prefix;
 
   // --- stable compaction: warp w owns offsets [w*per, (w+1)*per), read 32 at a time
   const int per = ((n + NW - 1) / NW + 31) / 32 * 32;
@@ -131,33 +148,47 @@ __device__ __forceinline__ void score_and_select(const Params& p, int b, const A
   for (int base = lo; base < hi; base += 32) {
     const int i = base + lane;
     const bool ok = i < hi;
-    const uint32_t key = ok ? keys[i] : 0u;
+    const uint32_t key = ok ? (keys[i] & mask) : 0u;
     gt += __popc(__ballot_sync(0xffffffffu, ok && key > thr));
     eq += __popc(__ballot_sync(0xffffffffu, ok && key == thr));
   }
+  int* s_gt = scratch + 4;
+  int* s_eq = scratch + 4 + NW;
   if (lane == 0) {
-    scratch[2 + warp] = gt;
-    scratch[2 + NW + warp] = eq;
+    s_gt[warp] = gt;
+    s_eq[warp] = eq;
   }
   __syncthreads();
-  int eq_before = 0, out_before = 0;
+  // exclusive scans over the warps, done by every warp with shuffles
+  int eq_before, out_before;
   {
-    int eb = 0;
-    for (int w = 0; w < NW; ++w) {
-      const int g_w = scratch[2 + w], e_w = scratch[2 + NW + w];
-      int take = krem - eb;
-      take = take < 0 ? 0 : (take > e_w ? e_w : take);
-      if (w < warp) out_before += g_w + take;
-      if (w == warp) eq_before = eb;
-      eb += e_w;
+    const int g_w = lane < NW ? s_gt[lane] : 0;
+    const int e_w = lane < NW ? s_eq[lane] : 0;
+    int e_incl = e_w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, e_incl, o);
+      if (lane >= o) e_incl += y;
     }
+    const int e_excl = e_incl - e_w;
+    int take = krem - e_excl;
+    take = take < 0 ? 0 : (take > e_w ? e_w : take);
+    int o_incl = g_w + take;
+    const int mine = o_incl;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, o_incl, o);
+      if (lane >= o) o_incl += y;
+    }
+    eq_before = __shfl_sync(0xffffffffu, e_excl, warp);
+    out_before = __shfl_sync(0xffffffffu, o_incl - mine, warp);
   }
   int32_t* dst = p.idx_out + (size_t)b * p.idx_stride;
   int eq_run = eq_before, out_run = out_before;
   for (int base = lo; base < hi; base += 32) {
     const int i = base + lane;
     const bool ok = i < hi;
-    const uint32_t key = ok ? keys[i] : 0u;
+    const uint32_t key = ok ? (keys[i] & mask) : 0u;
     const bool is_gt = ok && key > thr, is_eq = ok && key == thr;
     const uint32_t eq_b = __ballot_sync(0xffffffffu, is_eq);
     const int my_eq_rank = eq_run + __popc(eq_b & lt_mask);
@@ -185,8 +216,8 @@ __global__ void __launch_bounds__(NT) select_kernel(const Params p) {
 }
 
 inline int select_smem_bytes(int max_img) {
-  return TopkSmem::hist_offset(max_img) + 256 * 4 + (2 * (kSelectThreads / 32) + 4) * 4 +
-         (kSelectThreads / 32) * 8 + 16;
+  constexpr int NW = kSelectThreads / 32;
+  return TopkSmem::hist_offset(max_img) + 256 * 4 + 4 * 256 * 4 + (4 + 2 * NW) * 4 + NW * 8 + 16;
 }
 
 inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, int smem, cudaStream_t stream,
@@ -205,6 +236,96 @@ inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, int smem, cudaStream
 
 // ---------------------------------------------------------------- main kernel
 
+//
+// Work list of one CTA. The mode's attend set minus the current token N_t-1
+// is the "text" list (at most two contiguous position ranges); the S CTAs of a
+// (sequence, KV head) take equal contiguous shares of it, the last CTA also
+// takes the current token, and in sparse mode every CTA takes an equal share
+// of the selection. Text entries -- cache rows of earlier tokens, their
+// pages, the lengths -- are final before the previous kernel on the stream
+// starts, so they are resolved and their first tiles staged into shared
+// memory before griddepcontrol.wait; the current token, the selection and q
+// are read only after it.
+struct CtaList {
+  int n_t;
+  int a1, len1, a2, len2;   // text ranges [a1, a1+len1) and [a2, a2+len2)
+  int txt_lo, n_txt;        // this CTA's text entries
+  int has_cur, cur_pos;     // this CTA attends the current token
+  const int32_t* sel;       // sparse: selected positions of this sequence
+  int sel_lo, n_sel;        // this CTA's selection entries
+  int img_start, n_img;
+};
+
+template <int MODE>
+__device__ __forceinline__ CtaList make_cta_list(const Params& p, int b, int split, int& bad) {
+  CtaList c;
+  const AttendList L = make_list<MODE>(p, b, bad);   // lengths and image range (not k)
+  const int n_t = L.n_t;
+  c.n_t = n_t;
+  c.img_start = L.img_start;
+  c.n_img = L.n_img;
+  c.sel = L.sel;
+  c.sel_lo = 0;
+  c.n_sel = 0;
+  const int cur = n_t - 1;
+  int a1 = 0, len1 = 0, a2 = 0, len2 = 0, in_set = 0;
+  if (n_t >= 1) {
+    if (MODE == kFull || MODE == kFocal) {
+      len1 = n_t - 1;
+      in_set = 1;
+    } else if (MODE == kRswa) {
+      const int pre = min(p.prefix_len, n_t);
+      if (cur < p.prefix_len) {
+        len1 = cur;
+        in_set = 1;
+      } else {
+        len1 = pre;
+        a2 = max(p.prefix_len, n_t - p.window);
+        len2 = max(0, cur - a2);
+        in_set = p.window >= 1;
+      }
+    } else {  // kSparse: prefix [0, start) and generated [start + N_img, N_t)
+      const int tail = L.img_start + L.n_img;
+      if (cur >= tail) {
+        len1 = L.img_start;
+        a2 = tail;
+        len2 = cur - tail;
+        in_set = 1;
+      } else if (cur < L.img_start) {
+        len1 = cur;
+        in_set = 1;
+      } else {
+        len1 = L.img_start;
+      }
+    }
+  }
+  c.a1 = a1;
+  c.len1 = len1;
+  c.a2 = a2;
+  c.len2 = len2;
+  const int n_text = len1 + len2;
+  const int per = (n_text + p.splits - 1) / p.splits;
+  c.txt_lo = split * per;
+  c.n_txt = max(0, min(per, n_text - c.txt_lo));
+  c.has_cur = in_set && split == p.splits - 1;
+  c.cur_pos = cur;
+  return c;
+}
+
+// Selection share of this CTA (sparse), after the previous kernel completed.
+__device__ __forceinline__ void add_selection(const Params& p, int b, int split, CtaList& c,
+                                              int& bad) {
+  int k = __ldcg(p.k_in + b);
+  const int k_cap = min(c.n_img, p.idx_stride);
+  if (k < 0 || k > k_cap) {
+    bad |= kDevBadSelection;
+    k = k < 0 ? 0 : k_cap;
+  }
+  const int per = (k + p.splits - 1) / p.splits;
+  c.sel_lo = split * per;
+  c.n_sel = max(0, min(per, k - c.sel_lo));
+}
+
 template <typename T, int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -222,97 +343,73 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
   const T* __restrict__ vg = static_cast<const T*>(p.v);
   const int32_t* __restrict__ bt = p.block_table + (size_t)b * p.max_pages;
   const int page_mask = (1 << p.log2_page) - 1;
-
-  // While the previous kernel on the stream may still run (programmatic
-  // dependent launch), warm L2 with this CTA's K/V rows, computed from a
-  // speculative read of the lengths, block table and selection. These reads
-  // only choose prefetch addresses (validated, never used for results), and
-  // every global read below bypasses L1, so stale values cannot leak in.
-  {
-    int ignore = 0;
-    const AttendList Ls = make_list<MODE>(p, b, ignore);
-    int ch = (Ls.n_att + p.splits - 1) / p.splits;
-    ch = (ch + kTile - 1) / kTile * kTile;
-    const int lo = split * ch, hi = min(Ls.n_att, lo + ch);
-    const uint32_t page_bytes = (uint32_t)(D * sizeof(T)) << p.log2_page;
-    auto prefetch_positions = [&](int pos_lo, int pos_hi) {
-      if (pos_hi <= pos_lo) return;
-      const int pg1 = (pos_hi - 1) >> p.log2_page;
-      for (int j = (pos_lo >> p.log2_page) + tid; j <= pg1; j += kThreads) {
-        const int page = __ldcg(bt + j);
-        if (page >= 0 && page < p.num_pages) {
-          const size_t off = ((size_t)page * p.Hkv + hkv) * ((size_t)D << p.log2_page);
-          prefetch_l2(kg + off, page_bytes);
-          prefetch_l2(vg + off, page_bytes);
-        }
-      }
-    };
-    prefetch_positions(lo, min(hi, Ls.n_pre));
-    const int sel_end = Ls.n_pre + Ls.n_sel;
-    if (MODE == kSparse) {
-      for (int v = max(lo, Ls.n_pre) + tid; v < min(hi, sel_end); v += kThreads) {
-        const int pos = __ldcg(Ls.sel + (v - Ls.n_pre));
-        if (pos < Ls.img_start || pos >= Ls.img_start + Ls.n_img) continue;
-        const int page = __ldcg(bt + (pos >> p.log2_page));
-        if (page < 0 || page >= p.num_pages) continue;
-        const size_t off =
-            ((((size_t)page * p.Hkv + hkv) << p.log2_page) | (size_t)(pos & page_mask)) * D;
-        prefetch_l2(kg + off, D * sizeof(T));
-        prefetch_l2(vg + off, D * sizeof(T));
-      }
-    }
-    const int t_lo = max(lo, sel_end), t_hi = hi;
-    if (t_hi > t_lo)
-      prefetch_positions(Ls.tail_start + (t_lo - sel_end), Ls.tail_start + (t_hi - sel_end));
-  }
-
-  // wait until the previous kernel on the stream has completed and its
-  // writes are visible (no-op when launched without the PDL attribute)
-  asm volatile("griddepcontrol.wait;\n" ::: "memory");
-  if (p.pdl_early) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  int bad = 0;
-  const AttendList L = make_list<MODE>(p, b, bad);
-
-  // this CTA's slice [r_lo, r_hi) of the attend list
-  int chunk = (L.n_att + p.splits - 1) / p.splits;
-  chunk = (chunk + kTile - 1) / kTile * kTile;
-  const int r_lo = split * chunk;
-  const int r_hi = min(L.n_att, r_lo + chunk);
-
   unsigned char* pipe = smem + warp * kStages * SM::kStageBytes;
   int* srow = reinterpret_cast<int*>(smem + SM::kRowOffset);
+  int* spos = reinterpret_cast<int*>(smem + SM::kPosOffset);
 
-  // Resolve list entries [rlo, rhi) (at most kSliceMax) to cache rows
-  // (page * H_kv + hkv) * page_size + slot, -1 if masked, into shared memory.
-  // All lookups of a thread are issued before any is used, so a round costs
-  // two memory latencies (selection, then block table) instead of two per tile.
-  auto resolve = [&](int rlo, int rhi) {
+  // announce this CTA to its cluster (the partial exchange waits for it)
+  cluster_arrive_relaxed();
+
+  int bad = 0;
+  CtaList c = make_cta_list<MODE>(p, b, split, bad);
+
+  // cache position of work-list entry u (-1: masked)
+  // The text entries are padded to whole tiles (n_txt_pad), so that a tile
+  // never mixes text with late entries and every text tile can be staged
+  // before the wait; padding entries are masked.
+  const int n_txt_pad = (c.n_txt + kTile - 1) / kTile * kTile;
+  auto pos_of = [&](int u) -> int {
+    if (u < n_txt_pad) {
+      if (u >= c.n_txt) return -1;
+      const int t = c.txt_lo + u;
+      return t < c.len1 ? c.a1 + t : c.a2 + (t - c.len1);
+    }
+    u -= n_txt_pad;
+    if (c.has_cur) {
+      if (u == 0) return c.cur_pos;
+      u -= 1;
+    }
+    const int pos = __ldcg(c.sel + c.sel_lo + u);
+    if (pos < c.img_start || pos >= c.img_start + c.n_img) {
+      bad |= kDevBadSelection;
+      return -1;
+    }
+    return pos;
+  };
+
+  // Resolve entries [u0, u1) of the round starting at entry rb into cache rows
+  // (page*H_kv + hkv)*page_size + slot (-1: masked) and positions; every
+  // lookup of a thread is issued before any is used.
+  auto resolve = [&](int rb, int u0, int u1) {
     constexpr int kPer = kSliceMax / kThreads;
     int pos[kPer], page[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-      const int v = rlo + tid + j * kThreads;
-      pos[j] = v < rhi ? list_pos<MODE>(L, v, bad) : -1;
+      const int u = u0 + tid + j * kThreads;
+      pos[j] = u < u1 ? pos_of(u) : -1;
     }
 #pragma unroll
     for (int j = 0; j < kPer; ++j) page[j] = pos[j] >= 0 ? __ldcg(bt + (pos[j] >> p.log2_page)) : -1;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-      const int v = rlo + tid + j * kThreads;
-      if (v >= rhi) continue;
-      int row = -1;
-      if (pos[j] >= 0) {
-        if (page[j] < 0 || page[j] >= p.num_pages)
+      const int u = u0 + tid + j * kThreads;
+      if (u >= u1) continue;
+      int row = -1, ps = pos[j];
+      if (ps >= 0) {
+        if (page[j] < 0 || page[j] >= p.num_pages) {
           bad |= kDevBadPage;
-        else
-          row = ((page[j] * p.Hkv + hkv) << p.log2_page) | (pos[j] & page_mask);
+          ps = -1;
+        } else {
+          row = ((page[j] * p.Hkv + hkv) << p.log2_page) | (ps & page_mask);
+        }
       }
-      srow[v - rlo] = row;
+      srow[u - rb] = row;
+      spos[u - rb] = ps;
     }
   };
 
-  // Stage tile j (of this warp, within the current round) into its pipeline
-  // slot: 2 x 16 rows in 16-byte chunks, each instruction covering whole rows.
+  // Stage tile j of this warp in the current round: 2 x 16 rows in 16-byte
+  // chunks, each instruction covering whole rows.
   auto issue = [&](int j, int n_round) {
     const int stage = j % kStages;
     const int base = (warp + j * kWarps) * kTile;
@@ -324,9 +421,9 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
     const uint32_t sb = smem_u32(pipe + stage * SM::kStageBytes);
 #pragma unroll
     for (int i = 0; i < 2 * kTile * CH / 32; ++i) {
-      const int c = i * 32 + lane;
-      const int kv = c / (kTile * CH);
-      const int rem = c % (kTile * CH);
+      const int cc = i * 32 + lane;
+      const int kv = cc / (kTile * CH);
+      const int rem = cc % (kTile * CH);
       const int row = rem / CH, ch = rem % CH;
       const long long ro = __shfl_sync(0xffffffffu, rowoff, row);
       const T* src = (kv == 0 ? kg : vg) + (ro < 0 ? 0 : ro) + ch * kElemPerChunk;
@@ -335,11 +432,63 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
     }
   };
 
+  // ---------------- before the previous kernel completes: text entries of round 0
+  const int n_txt0 = min(n_txt_pad, kSliceMax);
+  resolve(0, 0, n_txt0);
+  __syncthreads();
+  int pre_issued = 0;   // leading tiles of this warp already staged
+#pragma unroll
+  for (int j = 0; j < kStages - 1; ++j) {
+    const int end = (warp + j * kWarps + 1) * kTile;   // tile must hold text entries only
+    if (pre_issued == j && end <= n_txt0) {
+      issue(j, n_txt0);
+      cp_async_commit();
+      ++pre_issued;
+    }
+  }
+
+  // The next kAhead tiles of every warp beyond the staged ones, and
+  // (speculatively) the selected image rows: pull them into L2 while waiting.
+  // Prefetches only warm the cache; the selection is read again after the wait.
+  {
+    const int u_end = min(n_txt0, kWarps * (kStages - 1 + kAhead) * kTile);
+    for (int u = kWarps * (kStages - 1) * kTile + tid; u < u_end; u += kThreads) {
+      const int row = srow[u];
+      if (row >= 0) {
+        prefetch_l2(kg + (size_t)row * D, ROWB);
+        prefetch_l2(vg + (size_t)row * D, ROWB);
+      }
+    }
+  }
+  if (MODE == kSparse) {
+    int k = __ldcg(p.k_in + b);
+    k = max(0, min(k, min(c.n_img, p.idx_stride)));
+    const int per = (k + p.splits - 1) / p.splits;
+    const int lo = split * per, hi = min(k, lo + per);
+    for (int v = lo + tid; v < hi; v += kThreads) {
+      const int pos = __ldcg(c.sel + v);
+      if (pos < c.img_start || pos >= c.img_start + c.n_img) continue;
+      const int page = __ldcg(bt + (pos >> p.log2_page));
+      if (page < 0 || page >= p.num_pages) continue;
+      const size_t row = ((((size_t)page * p.Hkv + hkv) << p.log2_page) | (size_t)(pos & page_mask));
+      prefetch_l2(kg + row * D, ROWB);
+      prefetch_l2(vg + row * D, ROWB);
+    }
+  }
+
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  if (p.pdl_early) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+
+  // ---------------- after it: selection, current token, q
+  if (MODE == kSparse) add_selection(p, b, split, c, bad);
+  const int n_cta = n_txt_pad + c.has_cur + c.n_sel;
+  const int n_round0 = min(n_cta, kSliceMax);
+  if (n_round0 > n_txt0) resolve(0, n_txt0, n_round0);
+
   float* logit_base = nullptr;
   if (MODE == kFocal)
     logit_base = p.logits + ((size_t)b * p.Hkv + hkv) * (size_t)p.max_img * kSlots;
 
-  // ---------------- per-warp streaming
   WarpStateMma<D> sm_;
   WarpStateF32<D> sf_;
   const int gid = lane >> 2, tig = lane & 3;
@@ -354,14 +503,14 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
     const T* qrow = static_cast<const T*>(p.q) + ((size_t)b * p.Hq + hkv * p.g + (have ? gid : 0)) * D;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-      sm_.qf[ks][0] = have ? __ldcg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * tig)) : 0u;
-      sm_.qf[ks][1] = have ? __ldcg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * tig)) : 0u;
+      sm_.qf[ks][0] = have ? __ldcg(reinterpret_cast<const unsigned int*>(qrow + 16 * ks + 2 * tig)) : 0u;
+      sm_.qf[ks][1] = have ? __ldcg(reinterpret_cast<const unsigned int*>(qrow + 16 * ks + 8 + 2 * tig)) : 0u;
     }
   } else {
     float* qs = reinterpret_cast<float*>(smem + SM::kQOffset);
     for (int e = tid; e < kSlots * D; e += kThreads) {
       const int h = e / D, d = e % D;
-      qs[e] = h < p.g ? static_cast<const float*>(p.q)[((size_t)b * p.Hq + hkv * p.g + h) * D + d] : 0.f;
+      qs[e] = h < p.g ? __ldcg(static_cast<const float*>(p.q) + ((size_t)b * p.Hq + hkv * p.g + h) * D + d) : 0.f;
     }
 #pragma unroll
     for (int h = 0; h < kSlots; ++h) {
@@ -370,159 +519,176 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
 #pragma unroll
       for (int j = 0; j < D / 32; ++j) sf_.acc[h][j] = 0.f;
     }
-    __syncthreads();
   }
-
-  for (int rlo = r_lo; rlo < r_hi; rlo += kSliceMax) {
-  const int n_round = min(r_hi - rlo, kSliceMax);
-  resolve(rlo, rlo + n_round);
   __syncthreads();
-  const int n_tiles = (n_round + kTile - 1) / kTile;
-  const int my_tiles = n_tiles > warp ? (n_tiles - warp + kWarps - 1) / kWarps : 0;
-#pragma unroll
-  for (int j = 0; j < kStages - 1; ++j) {
-    if (j < my_tiles) issue(j, n_round);
-    cp_async_commit();
-  }
-  for (int it = 0; it < my_tiles; ++it) {
-    if (it + kStages - 1 < my_tiles) issue(it + kStages - 1, n_round);
-    cp_async_commit();
-    cp_async_wait<kStages - 1>();
-    __syncwarp();
-    const int stage = it % kStages;
-    unsigned char* kS = pipe + stage * SM::kStageBytes;
-    unsigned char* vS = kS + kTile * ROWB;
-    const int tbase = (warp + it * kWarps) * kTile;    // tile start within the round
 
-    if constexpr (kMma) {
-      // S^T[16 keys x 8 heads] = K[16 x D] . Q^T[D x 8]
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t kA = smem_u32(kS), vA = smem_u32(vS);
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const int row = (lane & 7) + (lane & 8);
-        const int ch = 2 * ks + (lane >> 4);
-        uint32_t a[4];
-        ldmatrix_x4(a, kA + row * ROWB + ((ch ^ (row & 7)) << 4));
-        mma_bf16(c, a, sm_.qf[ks][0], sm_.qf[ks][1]);
-      }
-      // list position of tokens gid / gid+8 (= cache position in focal mode), -1 if masked
-      const int posA = (tbase + gid < n_round && srow[tbase + gid] >= 0) ? rlo + tbase + gid : -1;
-      const int posB = (tbase + gid + 8 < n_round && srow[tbase + gid + 8] >= 0) ? rlo + tbase + gid + 8 : -1;
-      const float s0 = posA >= 0 ? c[0] * p.scale_log2 : kNegInf;
-      const float s1 = posA >= 0 ? c[1] * p.scale_log2 : kNegInf;
-      const float s2 = posB >= 0 ? c[2] * p.scale_log2 : kNegInf;
-      const float s3 = posB >= 0 ? c[3] * p.scale_log2 : kNegInf;
-      if (MODE == kFocal) {
-        if (posA >= L.img_start && posA < L.img_start + L.n_img)
-          *reinterpret_cast<float2*>(logit_base + (size_t)(posA - L.img_start) * kSlots + 2 * tig) =
-              make_float2(s0, s1);
-        if (posB >= L.img_start && posB < L.img_start + L.n_img)
-          *reinterpret_cast<float2*>(logit_base + (size_t)(posB - L.img_start) * kSlots + 2 * tig) =
-              make_float2(s2, s3);
-      }
-      const float mx0 = warp_max_gid(fmaxf(s0, s2));
-      const float mx1 = warp_max_gid(fmaxf(s1, s3));
-      const float mn0 = fmaxf(sm_.m[0], mx0), mn1 = fmaxf(sm_.m[1], mx1);
-      const float b0f = mn0 == kNegInf ? 0.f : mn0, b1f = mn1 == kNegInf ? 0.f : mn1;
-      const float al0 = fast_exp2(sm_.m[0] - b0f), al1 = fast_exp2(sm_.m[1] - b1f);
-      const float p0 = fast_exp2(s0 - b0f), p2 = fast_exp2(s2 - b0f);
-      const float p1 = fast_exp2(s1 - b1f), p3 = fast_exp2(s3 - b1f);
-      sm_.l[0] = sm_.l[0] * al0 + (p0 + p2);
-      sm_.l[1] = sm_.l[1] * al1 + (p1 + p3);
-      sm_.m[0] = mn0;
-      sm_.m[1] = mn1;
-      // P^T[16 keys x 8 heads] as the B operand: transpose the two 8x8 blocks
-      const uint32_t bb0 = movmatrix_trans(pack_bf16(p0, p1));
-      const uint32_t bb1 = movmatrix_trans(pack_bf16(p2, p3));
-#pragma unroll
-      for (int mt = 0; mt < D / 16; ++mt) {
-        sm_.acc[mt][0] *= al0;
-        sm_.acc[mt][1] *= al1;
-        sm_.acc[mt][2] *= al0;
-        sm_.acc[mt][3] *= al1;
-        const int row = (lane & 7) + ((lane >> 4) << 3);
-        const int ch = 2 * mt + ((lane >> 3) & 1);
-        uint32_t a[4];
-        ldmatrix_x4_trans(a, vA + row * ROWB + ((ch ^ (row & 7)) << 4));
-        // O^T[16 dims x 8 heads] += V^T[16 dims x 16 keys] . P^T[16 keys x 8 heads]
-        mma_bf16(sm_.acc[mt], a, bb0, bb1);
-      }
+  // ---------------- stream the work list in rounds of kSliceMax entries
+  for (int rb = 0; rb < n_cta; rb += kSliceMax) {
+    const int n_round = min(n_cta - rb, kSliceMax);
+    int first = 0;            // tiles of this warp already staged for this round
+    if (rb > 0) {
+      resolve(rb, rb, rb + n_round);
+      __syncthreads();
     } else {
-      const float* qs = reinterpret_cast<const float*>(smem + SM::kQOffset);
-      const int r = lane & 15, half = lane >> 4;
-      float s[kSlots];
+      first = pre_issued;
+    }
+    const int n_tiles = (n_round + kTile - 1) / kTile;
+    const int my_tiles = n_tiles > warp ? (n_tiles - warp + kWarps - 1) / kWarps : 0;
 #pragma unroll
-      for (int h = 0; h < kSlots; ++h) s[h] = 0.f;
+    for (int j = 0; j < kStages - 1; ++j) {
+      if (j < first) continue;
+      if (j < my_tiles) issue(j, n_round);
+      cp_async_commit();
+    }
+    for (int it = 0; it < my_tiles; ++it) {
+      if (it + kStages - 1 < my_tiles) issue(it + kStages - 1, n_round);
+      cp_async_commit();
+      // keep this warp's tile kAhead beyond the pipeline on its way into L2
+      // (round 0 had its first kAhead such tiles prefetched before the wait)
+      {
+        const int ja = it + kStages - 1 + kAhead;
+        const int ua = (warp + ja * kWarps) * kTile + (lane & 15);
+        if (ja < my_tiles && ua < n_round) {
+          const int row = srow[ua];
+          if (row >= 0) prefetch_l2((lane < 16 ? kg : vg) + (size_t)row * D, ROWB);
+        }
+      }
+      cp_async_wait<kStages - 1>();
+      __syncwarp();
+      const int stage = it % kStages;
+      unsigned char* kS = pipe + stage * SM::kStageBytes;
+      unsigned char* vS = kS + kTile * ROWB;
+      const int tbase = (warp + it * kWarps) * kTile;   // tile start within the round
+
+      if constexpr (kMma) {
+        // S^T[16 keys x 8 heads] = K[16 x D] . Q^T[D x 8]
+        float cfr[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t kA = smem_u32(kS), vA = smem_u32(vS);
 #pragma unroll
-      for (int cc = 0; cc < CH / 2; ++cc) {
-        const int ch = half * (CH / 2) + cc;
-        const float4 kv = *reinterpret_cast<const float4*>(kS + r * ROWB + ((ch ^ (r & 7)) << 4));
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const int row = (lane & 7) + (lane & 8);
+          const int ch = 2 * ks + (lane >> 4);
+          uint32_t a[4];
+          ldmatrix_x4(a, kA + row * ROWB + ((ch ^ (row & 7)) << 4));
+          mma_bf16(cfr, a, sm_.qf[ks][0], sm_.qf[ks][1]);
+        }
+        // cache positions of keys gid and gid+8 (-1: masked or past the end)
+        const int posA = tbase + gid < n_round ? spos[tbase + gid] : -1;
+        const int posB = tbase + gid + 8 < n_round ? spos[tbase + gid + 8] : -1;
+        const float s0 = posA >= 0 ? cfr[0] * p.scale_log2 : kNegInf;
+        const float s1 = posA >= 0 ? cfr[1] * p.scale_log2 : kNegInf;
+        const float s2 = posB >= 0 ? cfr[2] * p.scale_log2 : kNegInf;
+        const float s3 = posB >= 0 ? cfr[3] * p.scale_log2 : kNegInf;
+        if (MODE == kFocal) {
+          if (posA >= c.img_start && posA < c.img_start + c.n_img)
+            *reinterpret_cast<float2*>(logit_base + (size_t)(posA - c.img_start) * kSlots + 2 * tig) =
+                make_float2(s0, s1);
+          if (posB >= c.img_start && posB < c.img_start + c.n_img)
+            *reinterpret_cast<float2*>(logit_base + (size_t)(posB - c.img_start) * kSlots + 2 * tig) =
+                make_float2(s2, s3);
+        }
+        const float mx0 = warp_max_gid(fmaxf(s0, s2));
+        const float mx1 = warp_max_gid(fmaxf(s1, s3));
+        const float mn0 = fmaxf(sm_.m[0], mx0), mn1 = fmaxf(sm_.m[1], mx1);
+        const float b0f = mn0 == kNegInf ? 0.f : mn0, b1f = mn1 == kNegInf ? 0.f : mn1;
+        const float al0 = fast_exp2(sm_.m[0] - b0f), al1 = fast_exp2(sm_.m[1] - b1f);
+        const float p0 = fast_exp2(s0 - b0f), p2 = fast_exp2(s2 - b0f);
+        const float p1 = fast_exp2(s1 - b1f), p3 = fast_exp2(s3 - b1f);
+        sm_.l[0] = sm_.l[0] * al0 + (p0 + p2);
+        sm_.l[1] = sm_.l[1] * al1 + (p1 + p3);
+        sm_.m[0] = mn0;
+        sm_.m[1] = mn1;
+        // P^T[16 keys x 8 heads] as the B operand: transpose the two 8x8 blocks
+        const uint32_t bb0 = movmatrix_trans(pack_bf16(p0, p1));
+        const uint32_t bb1 = movmatrix_trans(pack_bf16(p2, p3));
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          sm_.acc[mt][0] *= al0;
+          sm_.acc[mt][1] *= al1;
+          sm_.acc[mt][2] *= al0;
+          sm_.acc[mt][3] *= al1;
+          const int row = (lane & 7) + ((lane >> 4) << 3);
+          const int ch = 2 * mt + ((lane >> 3) & 1);
+          uint32_t a[4];
+          ldmatrix_x4_trans(a, vA + row * ROWB + ((ch ^ (row & 7)) << 4));
+          // O^T[16 dims x 8 heads] += V^T[16 dims x 16 keys] . P^T[16 keys x 8 heads]
+          mma_bf16(sm_.acc[mt], a, bb0, bb1);
+        }
+      } else {
+        const float* qs = reinterpret_cast<const float*>(smem + SM::kQOffset);
+        const int r = lane & 15, half = lane >> 4;
+        float s[kSlots];
+#pragma unroll
+        for (int h = 0; h < kSlots; ++h) s[h] = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < CH / 2; ++cc) {
+          const int ch = half * (CH / 2) + cc;
+          const float4 kv = *reinterpret_cast<const float4*>(kS + r * ROWB + ((ch ^ (r & 7)) << 4));
+#pragma unroll
+          for (int h = 0; h < kSlots; ++h) {
+            const float4 qv = *reinterpret_cast<const float4*>(qs + h * D + ch * 4);
+            s[h] = fmaf(kv.x, qv.x, s[h]);
+            s[h] = fmaf(kv.y, qv.y, s[h]);
+            s[h] = fmaf(kv.z, qv.z, s[h]);
+            s[h] = fmaf(kv.w, qv.w, s[h]);
+          }
+        }
+        const int pos = tbase + r < n_round ? spos[tbase + r] : -1;
 #pragma unroll
         for (int h = 0; h < kSlots; ++h) {
-          const float4 qv = *reinterpret_cast<const float4*>(qs + h * D + ch * 4);
-          s[h] = fmaf(kv.x, qv.x, s[h]);
-          s[h] = fmaf(kv.y, qv.y, s[h]);
-          s[h] = fmaf(kv.z, qv.z, s[h]);
-          s[h] = fmaf(kv.w, qv.w, s[h]);
+          s[h] += __shfl_xor_sync(0xffffffffu, s[h], 16);
+          s[h] = pos >= 0 ? s[h] * p.scale_log2 : kNegInf;
         }
-      }
-      const int pos = (tbase + r < n_round && srow[tbase + r] >= 0) ? rlo + tbase + r : -1;
-#pragma unroll
-      for (int h = 0; h < kSlots; ++h) {
-        s[h] += __shfl_xor_sync(0xffffffffu, s[h], 16);
-        s[h] = pos >= 0 ? s[h] * p.scale_log2 : kNegInf;
-      }
-      if (MODE == kFocal) {
-        if (half == 0 && pos >= L.img_start && pos < L.img_start + L.n_img) {
-          float* dst = logit_base + (size_t)(pos - L.img_start) * kSlots;
-          *reinterpret_cast<float4*>(dst) = make_float4(s[0], s[1], s[2], s[3]);
-          *reinterpret_cast<float4*>(dst + 4) = make_float4(s[4], s[5], s[6], s[7]);
+        if (MODE == kFocal) {
+          if (half == 0 && pos >= c.img_start && pos < c.img_start + c.n_img) {
+            float* dst = logit_base + (size_t)(pos - c.img_start) * kSlots;
+            *reinterpret_cast<float4*>(dst) = make_float4(s[0], s[1], s[2], s[3]);
+            *reinterpret_cast<float4*>(dst + 4) = make_float4(s[4], s[5], s[6], s[7]);
+          }
         }
-      }
-      float pr[kSlots];
+        float pr[kSlots];
 #pragma unroll
-      for (int h = 0; h < kSlots; ++h) {
-        float mx = s[h];
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        const float mn = fmaxf(sf_.m[h], mx);
-        const float base = mn == kNegInf ? 0.f : mn;
-        const float al = fast_exp2(sf_.m[h] - base);
-        pr[h] = fast_exp2(s[h] - base);
-        sf_.l[h] = sf_.l[h] * al + (half == 0 ? pr[h] : 0.f);
-        sf_.m[h] = mn;
+        for (int h = 0; h < kSlots; ++h) {
+          float mx = s[h];
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          const float mn = fmaxf(sf_.m[h], mx);
+          const float base = mn == kNegInf ? 0.f : mn;
+          const float al = fast_exp2(sf_.m[h] - base);
+          pr[h] = fast_exp2(s[h] - base);
+          sf_.l[h] = sf_.l[h] * al + (half == 0 ? pr[h] : 0.f);
+          sf_.m[h] = mn;
 #pragma unroll
-        for (int j = 0; j < D / 32; ++j) sf_.acc[h][j] *= al;
-      }
+          for (int j = 0; j < D / 32; ++j) sf_.acc[h][j] *= al;
+        }
 #pragma unroll 4
-      for (int tok = 0; tok < kTile; ++tok) {
-        float ph[kSlots];
+        for (int tok = 0; tok < kTile; ++tok) {
+          float ph[kSlots];
 #pragma unroll
-        for (int h = 0; h < kSlots; ++h) ph[h] = __shfl_sync(0xffffffffu, pr[h], tok);
+          for (int h = 0; h < kSlots; ++h) ph[h] = __shfl_sync(0xffffffffu, pr[h], tok);
 #pragma unroll
-        for (int j = 0; j < D / 32; ++j) {
-          const int d = lane + 32 * j;
-          const float v =
-              *reinterpret_cast<const float*>(vS + tok * ROWB + ((((d >> 2) ^ (tok & 7))) << 4) + (d & 3) * 4);
+          for (int j = 0; j < D / 32; ++j) {
+            const int d = lane + 32 * j;
+            const float v =
+                *reinterpret_cast<const float*>(vS + tok * ROWB + ((((d >> 2) ^ (tok & 7))) << 4) + (d & 3) * 4);
 #pragma unroll
-          for (int h = 0; h < kSlots; ++h) sf_.acc[h][j] = fmaf(ph[h], v, sf_.acc[h][j]);
+            for (int h = 0; h < kSlots; ++h) sf_.acc[h][j] = fmaf(ph[h], v, sf_.acc[h][j]);
+          }
         }
       }
+      __syncwarp();
     }
-    __syncwarp();
-  }
-  cp_async_wait<0>();
-  __syncthreads();   // before the next round overwrites the row list
+    cp_async_wait<0>();
+    __syncthreads();   // before the next round overwrites the row list
   }
   cp_async_wait<0>();
   // the next kernel may now be scheduled; it waits for this grid to finish
   if (!p.pdl_early) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   __syncthreads();
 
-  // ---------------- CTA merge of the four warps -> split partial
+  // ---------------- per-warp partials -> shared memory
   float* wm = reinterpret_cast<float*>(smem + E::kWm);
   float* wl = reinterpret_cast<float*>(smem + E::kWl);
   float* wacc = reinterpret_cast<float*>(smem + E::kWacc);
@@ -556,103 +722,129 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
       for (int j = 0; j < D / 32; ++j) wacc[(warp * kSlots + h) * D + lane + 32 * j] = sf_.acc[h][j];
     }
   }
+  if (bad) atomicOr(p.status, bad);
   __syncthreads();
 
-  // ---------------- this CTA's partial (m, l, acc) of every head slot, in shared memory
-  float* cm = reinterpret_cast<float*>(smem + E::kPartM);
-  float* cl = reinterpret_cast<float*>(smem + E::kPartL);
-  float* cacc = reinterpret_cast<float*>(smem + E::kPartAcc);
-  for (int e = tid; e < kSlots * D; e += kThreads) {
-    const int h = e / D, d = e % D;
+  // ---------------- CTA partial per head: max, sum, per-warp scales
+  float* cm = reinterpret_cast<float*>(smem + E::kCtaM);     // [8]
+  float* cl = reinterpret_cast<float*>(smem + E::kCtaL);     // [8]
+  float* csc = reinterpret_cast<float*>(smem + E::kCtaSc);   // [W][8]
+  if (tid < kSlots) {
+    const int h = tid;
     float M = kNegInf;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * kSlots + h]);
     const float base = M == kNegInf ? 0.f : M;
-    float A = 0.f, Ls = 0.f;
+    float Ls = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
       const float sc = fast_exp2(wm[w * kSlots + h] - base);
-      A = fmaf(wacc[(w * kSlots + h) * D + d], sc, A);
+      csc[w * kSlots + h] = sc;
       Ls = fmaf(wl[w * kSlots + h], sc, Ls);
     }
-    cacc[e] = A;
-    if (d == 0) {
-      cm[h] = M;
-      cl[h] = Ls;
-    }
+    cm[h] = M;
+    cl[h] = Ls;
   }
-  if (bad) atomicOr(p.status, bad);
-  // The CTAs of one (sequence, KV head) form a thread-block cluster; the split
-  // partials are merged through distributed shared memory. Global writes of
-  // this CTA (focal logits) are fenced before the cluster barrier so that the
-  // other CTAs of the cluster read them after it.
-  if (MODE == kFocal) __threadfence();
   __syncthreads();
-  cluster_sync();
 
-  const int S = p.splits;               // == cluster size
+  // ---------------- push the partial to the CTAs of the cluster
+  // CTA `r` of the S splits owns output pairs [r*per, (r+1)*per) of the
+  // (head, 4 dims) pairs; every CTA writes its share of each owner's pairs,
+  // and its per-head (max, sum), straight into the owner's shared memory.
+  const int S = p.splits;
   const uint32_t rank = cluster_ctarank();
+  constexpr int C4 = D / 4;
+  const int n_pairs = p.g * C4;
+  const int per = (n_pairs + S - 1) / S;
+  float* rml = reinterpret_cast<float*>(smem + SM::kRecvMl);     // [S][8][2]
+  float* racc = reinterpret_cast<float*>(smem + SM::kRecvAcc);   // [S][per][4]
+  cluster_wait();   // every CTA of the cluster has started (its receive area exists)
+  if (MODE == kFocal) __threadfence();   // logits of this CTA, read by others below
+  for (int e = tid; e < S * kSlots; e += kThreads) {
+    const int r = e / kSlots, h = e % kSlots;
+    st_dsmem_f32x2(rml + (rank * kSlots + h) * 2, r, cm[h], cl[h]);
+  }
+  for (int e = tid; e < n_pairs; e += kThreads) {
+    const int h = e / C4, c4 = e % C4;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float sc = csc[w * kSlots + h];
+      const float4 v = *reinterpret_cast<const float4*>(wacc + (w * kSlots + h) * D + 4 * c4);
+      a.x = fmaf(v.x, sc, a.x);
+      a.y = fmaf(v.y, sc, a.y);
+      a.z = fmaf(v.z, sc, a.z);
+      a.w = fmaf(v.w, sc, a.w);
+    }
+    const int r = e / per;
+    st_dsmem_f32x4(racc + ((size_t)rank * per + (e - r * per)) * 4, r, a);
+  }
+  cluster_sync();   // release the pushes, acquire everyone else's
+
+  // ---------------- owner: merge the S partials of its pairs (local memory only)
   float* sM = reinterpret_cast<float*>(smem + E::kM);
   float* sInvL = reinterpret_cast<float*>(smem + E::kInvL);
-  float* sScale = reinterpret_cast<float*>(smem + E::kScale);  // [S][8]
-  float* rml = reinterpret_cast<float*>(smem + E::kRemoteMl);   // [S][8][2]
-  for (int e = tid; e < S * kSlots; e += kThreads) {
-    const int s = e / kSlots, h = e % kSlots;
-    rml[2 * e] = ld_dsmem_f32(cm + h, s);
-    rml[2 * e + 1] = ld_dsmem_f32(cl + h, s);
-  }
-  __syncthreads();
-  if (tid < kSlots) {
-    const int h = tid;
-    float M = kNegInf;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, rml[2 * (s * kSlots + h)]);
+  float* sScale = reinterpret_cast<float*>(smem + E::kScale);   // [S][8]
+  // per-head max and sum over the S partials: warp w takes heads w and w+4,
+  // lane s reads partial s
+  for (int h = warp; h < kSlots; h += kWarps) {
+    const float ms = lane < S ? rml[(lane * kSlots + h) * 2] : kNegInf;
+    const float ls = lane < S ? rml[(lane * kSlots + h) * 2 + 1] : 0.f;
+    float M = ms;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float base = M == kNegInf ? 0.f : M;
-    float Ls = 0.f;
-    for (int s = 0; s < S; ++s)
-      Ls = fmaf(rml[2 * (s * kSlots + h) + 1], fast_exp2(rml[2 * (s * kSlots + h)] - base), Ls);
-    sM[h] = base;
-    sInvL[h] = Ls > 0.f ? __frcp_rn(Ls) : 0.f;
+    const float sc = lane < S ? fast_exp2(ms - base) : 0.f;
+    float Ls = ls * sc;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+    const float inv = Ls > 0.f ? __frcp_rn(Ls) : 0.f;
+    if (lane < S) sScale[lane * kSlots + h] = sc * inv;
+    if (lane == 0) {
+      sM[h] = base;
+      sInvL[h] = inv;
+    }
   }
   __syncthreads();
-  for (int e = tid; e < S * kSlots; e += kThreads) {
-    const int h = e % kSlots;
-    sScale[e] = fast_exp2(rml[2 * e] - sM[h]) * sInvL[h];
-  }
-  __syncthreads();
-
-  // ---------------- outputs: CTA `rank` owns a slice of the (head, 4-dim) pairs
   {
-    constexpr int C4 = D / 4;
-    const int n_pairs = p.g * C4;
-    const int per = (n_pairs + S - 1) / S;
-    const int e_hi = min(n_pairs, (int)(rank + 1) * per);
+    // G adjacent lanes share one output pair, each summing every G-th partial
     T* outp = static_cast<T*>(p.out) + ((size_t)b * p.Hq + (size_t)hkv * p.g) * D;
-    for (int e = (int)rank * per + tid; e < e_hi; e += kThreads) {
-      const int h = e / C4, c4 = e % C4;
+    const int e_lo = (int)rank * per, e_hi = min(n_pairs, e_lo + per);
+    const int n_mine = max(0, e_hi - e_lo);
+    int G = 1;
+    while (G * 2 <= S && G * 2 * n_mine <= kThreads && G < 16) G *= 2;
+    const int sub = tid % G;
+    for (int e = e_lo + tid / G; e < e_lo + ((n_mine + (kThreads / G) - 1) / (kThreads / G)) * (kThreads / G);
+         e += kThreads / G) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s0 = 0; s0 < S; s0 += 8) {
-        float4 v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          v[u] = s0 + u < S ? ld_dsmem_f32x4(cacc + h * D + 4 * c4, s0 + u)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float sc = s0 + u < S ? sScale[(s0 + u) * kSlots + h] : 0.f;
-          acc.x = fmaf(v[u].x, sc, acc.x);
-          acc.y = fmaf(v[u].y, sc, acc.y);
-          acc.z = fmaf(v[u].z, sc, acc.z);
-          acc.w = fmaf(v[u].w, sc, acc.w);
+      const bool ok = e < e_hi;
+      const int h = ok ? e / C4 : 0, c4 = ok ? e % C4 : 0;
+      if (ok) {
+        for (int s = sub; s < S; s += G) {
+          const float4 v = *reinterpret_cast<const float4*>(racc + ((size_t)s * per + (e - e_lo)) * 4);
+          const float sc = sScale[s * kSlots + h];
+          acc.x = fmaf(v.x, sc, acc.x);
+          acc.y = fmaf(v.y, sc, acc.y);
+          acc.z = fmaf(v.z, sc, acc.z);
+          acc.w = fmaf(v.w, sc, acc.w);
         }
       }
-      T* o = outp + h * D + 4 * c4;
-      if constexpr (kMma) {
-        uint2 w;
-        w.x = pack_bf16(acc.x, acc.y);
-        w.y = pack_bf16(acc.z, acc.w);
-        *reinterpret_cast<uint2*>(o) = w;
-      } else {
-        *reinterpret_cast<float4*>(o) = acc;
+      for (int o = 1; o < G; o <<= 1) {
+        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
+        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o);
+        acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o);
+        acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
+      }
+      if (ok && sub == 0) {
+        T* o = outp + h * D + 4 * c4;
+        if constexpr (kMma) {
+          uint2 w;
+          w.x = pack_bf16(acc.x, acc.y);
+          w.y = pack_bf16(acc.z, acc.w);
+          *reinterpret_cast<uint2*>(o) = w;
+        } else {
+          *reinterpret_cast<float4*>(o) = acc;
+        }
       }
     }
   }
@@ -667,8 +859,8 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
     }
     const size_t unit = (size_t)b * p.Hkv + hkv;
     float* sp = p.sigma_part + unit * p.max_img;
-    const int nper = (L.n_img + S - 1) / S;
-    const int i_lo = (int)rank * nper, i_hi = min(L.n_img, i_lo + nper);
+    const int nper = (c.n_img + S - 1) / S;
+    const int i_lo = (int)rank * nper, i_hi = min(c.n_img, i_lo + nper);
     for (int i0 = i_lo; i0 < i_hi; i0 += 4 * kThreads) {
       float4 x[4][2];
 #pragma unroll
@@ -691,8 +883,6 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
       }
     }
   }
-  // no CTA may leave while another still reads its shared memory
-  cluster_sync();
 }
 
 // Launch with programmatic dependent launch: the grid may be scheduled while

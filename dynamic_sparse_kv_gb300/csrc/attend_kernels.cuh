@@ -36,6 +36,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 16;      // tokens per warp tile
 constexpr int kSlots = 8;      // query-head slots per KV head (g <= 8)
 constexpr int kStages = 3;     // cp.async pipeline depth per warp
+constexpr int kAhead = 4;      // tiles per warp kept in flight to L2 beyond the pipeline
 constexpr int kMaxSplits = 16;  // = the largest thread-block cluster used
 constexpr int kMaxImg = 16384; // image tokens whose scores fit in shared memory
 
@@ -125,28 +126,29 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
   asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
+}
+// Store to the same shared-memory offset as `local` in CTA `rank` of the cluster.
+__device__ __forceinline__ void st_dsmem_f32x2(float* local, uint32_t rank, float a, float b) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};\n" ::"r"(remote), "f"(a), "f"(b) : "memory");
+}
+__device__ __forceinline__ void st_dsmem_f32x4(float* local, uint32_t rank, float4 v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(remote), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
   return r;
-}
-// Load from the same shared-memory offset as `local` in CTA `rank` of the cluster.
-__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(remote) : "memory");
-  return v;
-}
-__device__ __forceinline__ float4 ld_dsmem_f32x4(const float* local, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];\n"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(remote)
-               : "memory");
-  return v;
 }
 // Bring `bytes` (multiple of 16) at `p` into L2; never faults on a valid address.
 __device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
@@ -191,6 +193,8 @@ struct AttendList {
   int img_start, n_img;  // image range (focal: logits; sparse: selection check)
 };
 
+// Lengths and image range of sequence b (validated and clamped; faults are
+// ORed into `bad`). n_pre/n_att describe the full-cache list [0, N_t).
 template <int MODE>
 __device__ __forceinline__ AttendList make_list(const Params& p, int b, int& bad) {
   AttendList L;
@@ -201,6 +205,8 @@ __device__ __forceinline__ AttendList make_list(const Params& p, int b, int& bad
     n_t = n_t < 0 ? 0 : (n_t > cap ? cap : n_t);
   }
   L.n_t = n_t;
+  L.n_pre = n_t;
+  L.n_att = n_t;
   L.sel = nullptr;
   L.n_sel = 0;
   L.tail_start = 0;
@@ -217,53 +223,13 @@ __device__ __forceinline__ AttendList make_list(const Params& p, int b, int& bad
     L.img_start = s;
     L.n_img = n;
   }
-  if (MODE == kFull || MODE == kFocal) {
-    L.n_pre = n_t;
-    L.n_att = n_t;
-  } else if (MODE == kSparse) {
-    int k = __ldcg(p.k_in + b);
-    const int k_cap = L.n_img < p.idx_stride ? L.n_img : p.idx_stride;
-    if (k < 0 || k > k_cap) {
-      bad |= kDevBadSelection;
-      k = k < 0 ? 0 : k_cap;
-    }
-    L.n_pre = L.img_start;
-    L.sel = p.idx + (size_t)b * p.idx_stride;
-    L.n_sel = k;
-    L.tail_start = L.img_start + L.n_img;
-    L.n_att = L.n_pre + k + (n_t - L.tail_start);
-  } else {  // kRswa
-    L.n_pre = p.prefix_len < n_t ? p.prefix_len : n_t;
-    int ts = n_t - p.window;
-    L.tail_start = ts > p.prefix_len ? ts : p.prefix_len;
-    int n_tail = n_t - L.tail_start;
-    L.n_att = L.n_pre + (n_tail > 0 ? n_tail : 0);
-  }
+  if (MODE == kSparse) L.sel = p.idx + (size_t)b * p.idx_stride;
   return L;
-}
-
-// Cache position of list entry v, or -1 (masked) if it is invalid.
-template <int MODE>
-__device__ __forceinline__ int list_pos(const AttendList& L, int v, int& bad) {
-  if (v < L.n_pre) return v;
-  v -= L.n_pre;
-  if (MODE == kSparse) {
-    if (v < L.n_sel) {
-      int pos = __ldcg(L.sel + v);
-      if (pos < L.img_start || pos >= L.img_start + L.n_img) {
-        bad |= kDevBadSelection;
-        return -1;
-      }
-      return pos;
-    }
-    v -= L.n_sel;
-  }
-  return L.tail_start + v;
 }
 
 // ---------------------------------------------------------------- shared memory
 
-constexpr int kSliceMax = 2048;  // attend-list entries resolved to cache rows per round
+constexpr int kSliceMax = 1024;  // work-list entries resolved to cache rows per round
 
 template <typename T, int D>
 struct Smem {
@@ -271,26 +237,31 @@ struct Smem {
   static constexpr int kStageBytes = 2 * kTile * kRowBytes;          // K rows then V rows
   static constexpr int kPipeBytes = kWarps * kStages * kStageBytes;
   static constexpr int kRowOffset = kPipeBytes;                      // int row[kSliceMax]
-  static constexpr int kQOffset = kRowOffset + kSliceMax * 4;        // f32 path: q[8][D]
+  static constexpr int kPosOffset = kRowOffset + kSliceMax * 4;      // int pos[kSliceMax]
+  // partials pushed here by the other CTAs of the cluster (never overlaps
+  // the pipeline, which may still be in use when they arrive)
+  static constexpr int kRecvMl = kPosOffset + kSliceMax * 4;         // f32 [kMaxSplits][8][2]
+  static constexpr int kRecvAcc = kRecvMl + kMaxSplits * kSlots * 2 * 4;
+  static constexpr int kRecvAccFloats = 4 * (kSlots * D / 4 + kMaxSplits);
+  static constexpr int kQOffset = kRecvAcc + kRecvAccFloats * 4;     // f32 path: q[8][D]
   static constexpr int kMainBytes = kQOffset + (sizeof(T) == 4 ? kSlots * D * 4 : 0);
 };
 
 template <int D>
 struct EpiSmem {
-  // per-warp partials wm[W][8], wl[W][8], wacc[W][8][D]; the CTA partial
-  // (read by the other CTAs of the cluster) m[8], l[8], acc[8][D]; merge
-  // scratch M[8], invL[8], scale[kMaxSplits][8], remote (m,l)[kMaxSplits][8][2]
+  // reuses the pipeline area once streaming is done: per-warp partials
+  // wm[W][8], wl[W][8], wacc[W][8][D]; CTA max/sum/warp scales; the owner's
+  // merge scratch M[8], invL[8], scale[kMaxSplits][8]
   static constexpr int kWm = 0;
   static constexpr int kWl = kWm + kWarps * kSlots * 4;
   static constexpr int kWacc = kWl + kWarps * kSlots * 4;
-  static constexpr int kPartM = kWacc + kWarps * kSlots * D * 4;
-  static constexpr int kPartL = kPartM + kSlots * 4;
-  static constexpr int kPartAcc = kPartL + kSlots * 4;
-  static constexpr int kM = kPartAcc + kSlots * D * 4;
+  static constexpr int kCtaM = kWacc + kWarps * kSlots * D * 4;
+  static constexpr int kCtaL = kCtaM + kSlots * 4;
+  static constexpr int kCtaSc = kCtaL + kSlots * 4;
+  static constexpr int kM = kCtaSc + kWarps * kSlots * 4;
   static constexpr int kInvL = kM + kSlots * 4;
   static constexpr int kScale = kInvL + kSlots * 4;
-  static constexpr int kRemoteMl = kScale + kMaxSplits * kSlots * 4;
-  static constexpr int kBytes = kRemoteMl + kMaxSplits * kSlots * 2 * 4;
+  static constexpr int kBytes = kScale + kMaxSplits * kSlots * 4;
 };
 
 struct TopkSmem {
@@ -301,9 +272,8 @@ struct TopkSmem {
 
 template <typename T, int D>
 inline int attend_smem_bytes() {
-  int a = Smem<T, D>::kMainBytes;
-  int b = EpiSmem<D>::kBytes;
-  return a > b ? a : b;
+  static_assert(EpiSmem<D>::kBytes <= Smem<T, D>::kPipeBytes, "epilogue must fit the pipeline area");
+  return Smem<T, D>::kMainBytes;
 }
 
 // ---------------------------------------------------------------- warp reductions

@@ -47,6 +47,16 @@
  *  handle must be ordered (one stream, or events): the handle's workspace is
  *  reused by every call.
  *
+ *  Overlap with the preceding kernel: the kernels are launched with
+ *  programmatic dependent launch, so they may start while the kernel before
+ *  them on `stream` is still running. Until that kernel has completed they
+ *  read only seq_len, block_table, img_range and the K/V rows (and their
+ *  block-table entries) of positions below N_t - 1; q, the selection (idx,
+ *  k) and the current token's K/V row are read after it completes. So the
+ *  former must be written before the kernel preceding the call starts -- in
+ *  a decode step they are set once before the first layer -- while q, the
+ *  selection and the current token may come from the kernel right before.
+ *
  *  Errors: argument errors are detected on the host and returned as a
  *  negative status before anything is launched. Faults in device data (page
  *  id out of range, seq_len above capacity, selection outside the image,

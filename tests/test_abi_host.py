@@ -83,3 +83,14 @@ def test_create_without_gpu_reports_no_device(lib):
     d = N.fastocr_dims(1, 4, 2, 64, 1, 16, 8, 64, 2)
     h = ctypes.c_void_p()
     assert N.lib.fastocr_create(ctypes.byref(d), ctypes.byref(h)) == N.FASTOCR_ERR_NO_DEVICE
+
+
+def test_header_compiles_as_c_and_cpp():
+    import shutil
+    import subprocess
+    for comp, lang in (("gcc", "c"), ("g++", "c++")):
+        if shutil.which(comp) is None:
+            pytest.skip(f"{comp} not found")
+        r = subprocess.run([comp, "-fsyntax-only", "-Wall", "-Werror", "-x", lang, HEADER],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
