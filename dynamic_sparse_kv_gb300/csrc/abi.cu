@@ -17,6 +17,8 @@ cudaError_t prepare_bf16();
 cudaError_t prepare_f32();
 int max_cluster_bf16(int head_dim);
 int max_cluster_f32(int head_dim);
+int active_clusters_bf16(int head_dim, int cluster);
+int active_clusters_f32(int head_dim, int cluster);
 }  // namespace fastocr
 
 using namespace fastocr;
@@ -28,6 +30,7 @@ struct fastocr_handle {
   int log2_page;
   int split_override[3];
   int max_splits;   // largest thread-block cluster the device co-schedules (<= 16)
+  int active[kMaxSplits + 1];   // clusters of each size the device holds at once
   void* ws;
   size_t ws_bytes;
   float* logits;
@@ -48,31 +51,15 @@ int ilog2_exact(int x) {
   return (1 << l) == x ? l : -1;
 }
 
-// Split-K factor (= cluster size): minimise (waves of CTAs) / splits + a small
-// per-split merge cost, with 2 resident CTAs per SM, at most one 64-token
-// tile per split, and no more splits than one cluster holds.
-int auto_splits(const fastocr_handle* h) {
-  const long units = (long)h->dims.batch * h->dims.num_kv_heads;
-  const long slots = (long)h->num_sms * 2;
-  const long max_tokens = (long)h->dims.max_pages_per_seq << h->log2_page;
-  const int max_useful =
-      (int)std::max(1L, std::min<long>(h->max_splits, (max_tokens + 63) / 64));
-  int best = 1;
-  double best_cost = 1e300;
-  for (int s = 1; s <= max_useful; ++s) {
-    const long waves = (units * s + slots - 1) / slots;
-    const double cost = (double)waves / s + 0.004 * s;
-    if (cost < best_cost - 1e-12) {
-      best_cost = cost;
-      best = s;
-    }
-  }
-  return best;
+int splits_for(const fastocr_handle* h, int mode_slot, long len) {
+  const int o = h->split_override[mode_slot];
+  return o > 0 ? std::min(o, h->max_splits)
+               : choose_splits((long)h->dims.batch * h->dims.num_kv_heads, len, h->max_splits,
+                               h->active);
 }
 
-int splits_for(const fastocr_handle* h, int mode_slot) {
-  const int o = h->split_override[mode_slot];
-  return o > 0 ? std::min(o, h->max_splits) : auto_splits(h);
+long max_tokens(const fastocr_handle* h) {
+  return (long)h->dims.max_pages_per_seq << h->log2_page;
 }
 
 fastocr_status check_kv(const fastocr_handle* h, const fastocr_kv* kv) {
@@ -185,6 +172,9 @@ fastocr_status fastocr_create(const fastocr_dims* dims, fastocr_handle** out) {
   h->log2_page = log2_page;
   h->max_splits = d.dtype == FASTOCR_DTYPE_BF16 ? max_cluster_bf16(d.head_dim)
                                                 : max_cluster_f32(d.head_dim);
+  for (int c = 1; c <= h->max_splits; ++c)
+    h->active[c] = d.dtype == FASTOCR_DTYPE_BF16 ? active_clusters_bf16(d.head_dim, c)
+                                                 : active_clusters_f32(d.head_dim, c);
   h->ws_bytes = off;
   if (cudaMalloc(&h->ws, off) != cudaSuccess) {
     free(h);
@@ -220,7 +210,7 @@ fastocr_status fastocr_full_attend(fastocr_handle* h, const void* q, const fasto
   if (st != FASTOCR_OK) return st;
   if (!aligned16(q) || !aligned16(out)) return FASTOCR_ERR_ALIGN;
   Params p = base_params(h, q, kv, out);
-  p.splits = splits_for(h, 0);
+  p.splits = splits_for(h, 0, max_tokens(h));
   return launch(h, kFull, p, stream);
 }
 
@@ -243,7 +233,7 @@ fastocr_status fastocr_focal_attend(fastocr_handle* h, const void* q, const fast
   p.idx_stride = idx_stride;
   p.k_out = k_out;
   p.profile_layer = profile_layer;
-  p.splits = splits_for(h, 0);
+  p.splits = splits_for(h, 0, max_tokens(h));
   return launch(h, kFocal, p, stream);
 }
 
@@ -261,7 +251,9 @@ fastocr_status fastocr_sparse_attend(fastocr_handle* h, const void* q, const fas
   p.idx = idx;
   p.idx_stride = idx_stride;
   p.k_in = k;
-  p.splits = splits_for(h, 1);
+  // text tokens (cache minus the image) plus at most idx_stride selected ones
+  const long text = std::max(0L, max_tokens(h) - (long)h->dims.max_img_tokens);
+  p.splits = splits_for(h, 1, std::min(max_tokens(h), text + idx_stride));
   return launch(h, kSparse, p, stream);
 }
 
@@ -276,7 +268,7 @@ fastocr_status fastocr_rswa_attend(fastocr_handle* h, const void* q, const fasto
   Params p = base_params(h, q, kv, out);
   p.prefix_len = prefix_len;
   p.window = window;
-  p.splits = splits_for(h, 2);
+  p.splits = splits_for(h, 2, std::min(max_tokens(h), (long)prefix_len + window));
   return launch(h, kRswa, p, stream);
 }
 

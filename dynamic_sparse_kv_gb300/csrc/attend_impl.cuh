@@ -929,6 +929,29 @@ cudaError_t prepare_all_modes() {
                               select_smem_bytes(kMaxImg));
 }
 
+// How many clusters of `c` CTAs of this kernel the device holds at once (0 if
+// a cluster of that size cannot be scheduled).
+template <typename T, int D>
+int active_clusters(int c) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(c, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = attend_smem_bytes<T, D>();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = c;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, attend_kernel<T, D, kFull>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
 // Largest cluster (<= kMaxSplits) of this kernel that the device can co-schedule.
 template <typename T, int D>
 int max_cluster_size() {

@@ -276,6 +276,34 @@ inline int attend_smem_bytes() {
   return Smem<T, D>::kMainBytes;
 }
 
+// Split-K factor S (= cluster size) for `units` (sequence, KV head) pairs and
+// attend lists of at most `len` tokens; active[s] = clusters of s CTAs the
+// device holds at once. Model: a CTA streams its share of len/S tokens at
+// ~13 ns per token (a 512-byte K+V row at ~40 GB/s per CTA), slowed down when
+// a wave of CTAs together asks for more than HBM delivers; clusters run in
+// waves of active[S]; every doubling of the cluster adds ~1 us of merge and
+// barrier latency.
+inline int choose_splits(long units, long len, int max_splits, const int* active) {
+  const double ns_per_token = 13.0, cta_gbs = 40.0, hbm_gbs = 6500.0, us_per_doubling = 1.0;
+  if (len < 1) len = 1;
+  int best = 1;
+  double best_cost = 1e300;
+  for (int s = 1; s <= max_splits; ++s) {
+    const int act = active[s];
+    if (act < 1) continue;
+    const long waves = (units + act - 1) / act;
+    const long ctas_in_wave = (units < act ? units : (long)act) * s;
+    const double slow = ctas_in_wave * cta_gbs / hbm_gbs > 1.0 ? ctas_in_wave * cta_gbs / hbm_gbs : 1.0;
+    const double per_cta_us = ((len + s - 1) / s) * ns_per_token * 1e-3 * slow;
+    const double cost = waves * per_cta_us + us_per_doubling * log2((double)s);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
 // ---------------------------------------------------------------- warp reductions
 
 __device__ __forceinline__ float warp_max_gid(float x) {  // over lanes with equal lane%4

@@ -23,6 +23,8 @@ cudaError_t prepare_bf16();
 cudaError_t prepare_f32();
 int max_cluster_bf16(int head_dim);
 int max_cluster_f32(int head_dim);
+int active_clusters_bf16(int head_dim, int cluster);
+int active_clusters_f32(int head_dim, int cluster);
 }  // namespace fastocr
 
 using namespace fastocr;
@@ -43,6 +45,7 @@ struct DeviceState {
   float* scratch;      // device address of g_scratch on this device
   int num_sms;
   int max_cluster[2][2];  // [dtype][head_dim == 128]
+  int active[2][2][kMaxSplits + 1];  // clusters of each size held at once
 };
 DeviceState g_state[kMaxDevices];
 std::mutex g_mutex;
@@ -64,31 +67,15 @@ fastocr_status device_setup(int dev, DeviceState** out) {
     s.max_cluster[FASTOCR_DTYPE_F32][1] = max_cluster_f32(128);
     s.max_cluster[FASTOCR_DTYPE_BF16][0] = max_cluster_bf16(64);
     s.max_cluster[FASTOCR_DTYPE_BF16][1] = max_cluster_bf16(128);
+    for (int dt = 0; dt < 2; ++dt)
+      for (int wide = 0; wide < 2; ++wide)
+        for (int c = 1; c <= s.max_cluster[dt][wide]; ++c)
+          s.active[dt][wide][c] = dt == FASTOCR_DTYPE_BF16 ? active_clusters_bf16(wide ? 128 : 64, c)
+                                                          : active_clusters_f32(wide ? 128 : 64, c);
     s.ready = true;
   }
   *out = &s;
   return FASTOCR_OK;
-}
-
-// Same split rule as the handle-based calls: fewest waves per split plus a
-// small merge cost, bounded by the cluster size and one 64-token tile per split.
-int choose_splits(const fastocr_dims& d, int log2_page, int num_sms, int max_cluster) {
-  const long units = (long)d.batch * d.num_kv_heads;
-  const long slots = (long)num_sms * 2;
-  const long max_tokens = (long)d.max_pages_per_seq << log2_page;
-  const long cap = std::min<long>(max_cluster, (max_tokens + 63) / 64);
-  const int max_useful = (int)(cap < 1 ? 1 : cap);
-  int best = 1;
-  double best_cost = 1e300;
-  for (int s = 1; s <= max_useful; ++s) {
-    const long waves = (units * s + slots - 1) / slots;
-    const double cost = (double)waves / s + 0.004 * s;
-    if (cost < best_cost - 1e-12) {
-      best_cost = cost;
-      best = s;
-    }
-  }
-  return best;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -162,8 +149,10 @@ extern "C" fastocr_status fastocr_focal_attend_noalloc(
   p.profile_layer = -1;
   p.status = status;
   p.max_img = d.max_img_tokens;
-  p.splits = choose_splits(d, log2_page, st->num_sms,
-                           st->max_cluster[d.dtype][d.head_dim == 128 ? 1 : 0]);
+  // same split rule as fastocr_focal_attend
+  const int wide = d.head_dim == 128 ? 1 : 0;
+  p.splits = choose_splits((long)d.batch * d.num_kv_heads, (long)d.max_pages_per_seq << log2_page,
+                           st->max_cluster[d.dtype][wide], st->active[d.dtype][wide]);
   p.pdl_early = (long)p.splits * p.Hkv * p.B <= st->num_sms;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const cudaError_t e = d.dtype == FASTOCR_DTYPE_BF16 ? launch_bf16(d.head_dim, kFocal, p, cs)
