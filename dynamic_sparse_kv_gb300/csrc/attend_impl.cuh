@@ -312,10 +312,9 @@ __device__ __forceinline__ CtaList make_cta_list(const Params& p, int b, int spl
   return c;
 }
 
-// Selection share of this CTA (sparse), after the previous kernel completed.
-__device__ __forceinline__ void add_selection(const Params& p, int b, int split, CtaList& c,
+// Selection share of this CTA (sparse) for k selected positions.
+__device__ __forceinline__ void add_selection(const Params& p, int k, int split, CtaList& c,
                                               int& bad) {
-  int k = __ldcg(p.k_in + b);
   const int k_cap = min(c.n_img, p.idx_stride);
   if (k < 0 || k > k_cap) {
     bad |= kDevBadSelection;
@@ -460,45 +459,56 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
       }
     }
   }
+  // Sparse: resolve this CTA's share of the selection speculatively from the
+  // current k and idx (the previous kernel may still be writing them) and pull
+  // those rows into L2. After the wait every thread re-reads its entries and
+  // the CTA keeps the speculative rows only if nothing changed.
+  constexpr int kPer = kSliceMax / kThreads;
+  const int sel_u0 = n_txt_pad + c.has_cur;   // first selection entry of the work list
+  int spec_k = -1, spec_lo = 0, spec_u1 = sel_u0;
+  int spec_raw[kPer];
   if (MODE == kSparse) {
-    int k = __ldcg(p.k_in + b);
-    k = max(0, min(k, min(c.n_img, p.idx_stride)));
-    const int per = (k + p.splits - 1) / p.splits;
-    const int lo = split * per, hi = min(k, lo + per);
-    for (int v = lo + tid; v < hi; v += kThreads) {
-      const int pos = __ldcg(c.sel + v);
-      if (pos < c.img_start || pos >= c.img_start + c.n_img) continue;
-      const int page = __ldcg(bt + (pos >> p.log2_page));
-      if (page < 0 || page >= p.num_pages) continue;
-      const size_t row = ((((size_t)page * p.Hkv + hkv) << p.log2_page) | (size_t)(pos & page_mask));
-      prefetch_l2(kg + row * D, ROWB);
-      prefetch_l2(vg + row * D, ROWB);
+    const int k_cap = min(c.n_img, p.idx_stride);
+    spec_k = min(max(__ldcg(p.k_in + b), 0), k_cap);
+    const int per = (spec_k + p.splits - 1) / p.splits;
+    spec_lo = split * per;
+    const int n_sel = max(0, min(per, spec_k - spec_lo));
+    spec_u1 = min(kSliceMax, sel_u0 + n_sel);
+    int pos[kPer], page[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int u = sel_u0 + tid + j * kThreads;
+      spec_raw[j] = u < spec_u1 ? __ldcg(c.sel + spec_lo + (u - sel_u0)) : -1;
+      pos[j] = (u < spec_u1 && spec_raw[j] >= c.img_start && spec_raw[j] < c.img_start + c.n_img)
+                   ? spec_raw[j] : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) page[j] = pos[j] >= 0 ? __ldcg(bt + (pos[j] >> p.log2_page)) : -1;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int u = sel_u0 + tid + j * kThreads;
+      if (u >= spec_u1) continue;
+      int row = -1, ps = pos[j];
+      if (ps >= 0 && page[j] >= 0 && page[j] < p.num_pages) {
+        row = ((page[j] * p.Hkv + hkv) << p.log2_page) | (ps & page_mask);
+        prefetch_l2(kg + (size_t)row * D, ROWB);
+        prefetch_l2(vg + (size_t)row * D, ROWB);
+      } else {
+        ps = -1;
+      }
+      srow[u] = row;
+      spos[u] = ps;
     }
   }
 
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   if (p.pdl_early) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
-  // ---------------- after it: selection, current token, q
-  if (MODE == kSparse) add_selection(p, b, split, c, bad);
-  const int n_cta = n_txt_pad + c.has_cur + c.n_sel;
-  const int n_round0 = min(n_cta, kSliceMax);
-  if (n_round0 > n_txt0) resolve(0, n_txt0, n_round0);
-
-  float* logit_base = nullptr;
-  if (MODE == kFocal)
-    logit_base = p.logits + ((size_t)b * p.Hkv + hkv) * (size_t)p.max_img * kSlots;
-
+  // ---------------- after it: q, selection, current token (loads issued together)
   WarpStateMma<D> sm_;
   WarpStateF32<D> sf_;
   const int gid = lane >> 2, tig = lane & 3;
   if constexpr (kMma) {
-#pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sm_.acc[mt][e] = 0.f;
-    sm_.m[0] = sm_.m[1] = kNegInf;
-    sm_.l[0] = sm_.l[1] = 0.f;
     const bool have = gid < p.g;
     const T* qrow = static_cast<const T*>(p.q) + ((size_t)b * p.Hq + hkv * p.g + (have ? gid : 0)) * D;
 #pragma unroll
@@ -506,6 +516,64 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
       sm_.qf[ks][0] = have ? __ldcg(reinterpret_cast<const unsigned int*>(qrow + 16 * ks + 2 * tig)) : 0u;
       sm_.qf[ks][1] = have ? __ldcg(reinterpret_cast<const unsigned int*>(qrow + 16 * ks + 8 + 2 * tig)) : 0u;
     }
+  }
+  int cur_page = -1;
+  if (c.has_cur && tid == 0 && n_txt_pad < kSliceMax) cur_page = __ldcg(bt + (c.cur_pos >> p.log2_page));
+  bool keep_spec = true;
+  if (MODE == kSparse) {
+    const int k = __ldcg(p.k_in + b);
+    int raw2[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int u = sel_u0 + tid + j * kThreads;
+      raw2[j] = u < spec_u1 ? __ldcg(c.sel + spec_lo + (u - sel_u0)) : -1;
+    }
+    add_selection(p, k, split, c, bad);
+    int ok = c.sel_lo == spec_lo && min(kSliceMax, sel_u0 + c.n_sel) == spec_u1;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int u = sel_u0 + tid + j * kThreads;
+      if (u < spec_u1 && raw2[j] != spec_raw[j]) ok = 0;
+    }
+    keep_spec = __syncthreads_and(ok) != 0;
+    if (keep_spec) {   // the speculative entries are the real ones: report the faulty ones
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int u = sel_u0 + tid + j * kThreads;
+        if (u >= spec_u1) continue;
+        if (raw2[j] < c.img_start || raw2[j] >= c.img_start + c.n_img)
+          bad |= kDevBadSelection;
+        else if (spos[u] < 0)
+          bad |= kDevBadPage;
+      }
+    }
+  }
+  if (cur_page >= 0 || (c.has_cur && tid == 0 && n_txt_pad < kSliceMax)) {
+    int row = -1, ps = c.cur_pos;
+    if (cur_page >= 0 && cur_page < p.num_pages) {
+      row = ((cur_page * p.Hkv + hkv) << p.log2_page) | (ps & page_mask);
+    } else {
+      bad |= kDevBadPage;
+      ps = -1;
+    }
+    srow[n_txt_pad] = row;
+    spos[n_txt_pad] = ps;
+  }
+  const int n_cta = n_txt_pad + c.has_cur + c.n_sel;
+  const int n_round0 = min(n_cta, kSliceMax);
+  if (!keep_spec && n_round0 > sel_u0) resolve(0, sel_u0, n_round0);
+
+  float* logit_base = nullptr;
+  if (MODE == kFocal)
+    logit_base = p.logits + ((size_t)b * p.Hkv + hkv) * (size_t)p.max_img * kSlots;
+
+  if constexpr (kMma) {
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sm_.acc[mt][e] = 0.f;
+    sm_.m[0] = sm_.m[1] = kNegInf;
+    sm_.l[0] = sm_.l[1] = 0.f;
   } else {
     float* qs = reinterpret_cast<float*>(smem + SM::kQOffset);
     for (int e = tid; e < kSlots * D; e += kThreads) {
@@ -561,8 +629,10 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
       const int tbase = (warp + it * kWarps) * kTile;   // tile start within the round
 
       if constexpr (kMma) {
-        // S^T[16 keys x 8 heads] = K[16 x D] . Q^T[D x 8]
-        float cfr[4] = {0.f, 0.f, 0.f, 0.f};
+        // S^T[16 keys x 8 heads] = K[16 x D] . Q^T[D x 8], two independent
+        // accumulation chains (even / odd 16-wide slices of d) to halve the
+        // dependent MMA latency
+        float ce[4] = {0.f, 0.f, 0.f, 0.f}, co[4] = {0.f, 0.f, 0.f, 0.f};
         const uint32_t kA = smem_u32(kS), vA = smem_u32(vS);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
@@ -570,8 +640,9 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
           const int ch = 2 * ks + (lane >> 4);
           uint32_t a[4];
           ldmatrix_x4(a, kA + row * ROWB + ((ch ^ (row & 7)) << 4));
-          mma_bf16(cfr, a, sm_.qf[ks][0], sm_.qf[ks][1]);
+          mma_bf16((ks & 1) ? co : ce, a, sm_.qf[ks][0], sm_.qf[ks][1]);
         }
+        const float cfr[4] = {ce[0] + co[0], ce[1] + co[1], ce[2] + co[2], ce[3] + co[3]};
         // cache positions of keys gid and gid+8 (-1: masked or past the end)
         const int posA = tbase + gid < n_round ? spos[tbase + gid] : -1;
         const int posB = tbase + gid + 8 < n_round ? spos[tbase + gid + 8] : -1;
