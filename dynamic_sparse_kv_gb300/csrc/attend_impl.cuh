@@ -10,27 +10,51 @@ namespace fastocr {
 
 // ---------------------------------------------------------------- top-k
 
-// Image scores and selection of sequence b, run by one CTA of NT threads:
-// sum the per-KV-head partial scores into keys (shared memory) in head order,
-// add the image mass to the profiler (warm-up only), and select the k largest
-// keys (ties to the lower offset) with an 8-bit radix select over the fp32
-// bit patterns (scores are >= 0, so the unsigned order is the float order).
-// The selection is written in ascending position order.
-template <int NT>
-__device__ __forceinline__ void score_and_select(const Params& p, int b, const AttendList& L,
-                                                 unsigned char* smem) {
-  constexpr int NW = NT / 32;
-  constexpr int kSub = 4;                                       // sub-histograms
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = L.n_img;
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
-  int* hist = reinterpret_cast<int*>(smem + TopkSmem::hist_offset(p.max_img));   // [256]
-  int* sub = hist + 256;                                        // [kSub][256]
-  int* scratch = sub + kSub * 256;                              // [4 + 2*NW]
-  double* dscr = reinterpret_cast<double*>(scratch + 4 + 2 * NW);  // [NW]
+constexpr int kSelectThreads = 1024;
+constexpr int kSelSub = 4;   // sub-histograms per radix pass (warp w counts into w % 4)
 
+// Shared memory of the selection kernel: keys[max_img] (fp32 bit patterns),
+// then the histograms of the four radix passes [4][kSelSub][256] (zeroed
+// before the kernel waits for its predecessor), then scratch.
+struct SelectSmem {
+  static constexpr int kNW = kSelectThreads / 32;
+  __host__ __device__ static int hist_offset(int max_img) { return (max_img * 4 + 15) / 16 * 16; }
+  __host__ __device__ static int scratch_offset(int max_img) { return hist_offset(max_img) + 4 * kSelSub * 256 * 4; }
+  __host__ __device__ static int bytes(int max_img) { return scratch_offset(max_img) + (8 + 2 * kNW) * 4 + kNW * 8 + 16; }
+};
+
+// Selection kernel of a focal layer: one CTA of NT threads per sequence,
+// launched right after the focal attend kernel, which left each KV head's
+// share of the image scores in the workspace. It sums the shares into keys in
+// a fixed head order, adds the image mass to the profiler slot (warm-up only),
+// and selects the k largest keys (ties to the lower offset) with an 8-bit
+// radix select over the fp32 bit patterns (scores are >= 0, so the unsigned
+// order is the float order); the first pass is counted while the keys are
+// summed, and the search stops as soon as every key sharing the decided prefix
+// is kept. The selection is written in ascending position order.
+template <int NT>
+__global__ void __launch_bounds__(NT) select_kernel(const Params p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  constexpr int NW = NT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
+  int* hist = reinterpret_cast<int*>(smem + SelectSmem::hist_offset(p.max_img));   // [4][kSelSub][256]
+  int* scratch = reinterpret_cast<int*>(smem + SelectSmem::scratch_offset(p.max_img));
+  double* dscr = reinterpret_cast<double*>(scratch + 8 + 2 * NW);
+  for (int i = tid; i < 4 * kSelSub * 256; i += NT) hist[i] = 0;
+
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  int bad = 0;  // already reported by the attend kernel
+  const AttendList L = make_list<kFocal>(p, b, bad);
+  const int n = L.n_img;
+  __syncthreads();   // histograms zeroed
+
+  // keys = sum of the KV heads' shares (fixed order); first-pass histogram
   const bool profiling = p.profile_layer >= 0;
   double local = 0.0;
+  int* h0 = hist + (warp & (kSelSub - 1)) * 256;
   const float* sp_b = p.sigma_part + (size_t)b * p.Hkv * p.max_img;
   for (int i0 = 0; i0 < n; i0 += 4 * NT) {
     float sv[4] = {0.f, 0.f, 0.f, 0.f};
@@ -52,10 +76,15 @@ __device__ __forceinline__ void score_and_select(const Params& p, int b, const A
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + u * NT + tid;
-      if (i < n) {
-        keys[i] = __float_as_uint(sv[u]);
+      const bool act = i < n;
+      const uint32_t key = __float_as_uint(sv[u]);
+      if (act) {
+        keys[i] = key;
         if (profiling) local += (double)sv[u];
       }
+      const uint32_t dig = act ? (key >> 24) : 256u;
+      const uint32_t same = __match_any_sync(0xffffffffu, dig);
+      if (act && lane == __ffs(same) - 1) atomicAdd(h0 + dig, __popc(same));
     }
   }
   if (profiling) {
@@ -77,38 +106,35 @@ __device__ __forceinline__ void score_and_select(const Params& p, int b, const A
   const int k = scratch[2];
   if (k == 0) return;
 
-  // --- radix select: find the k-th largest key, or stop early once every key
-  // sharing the decided prefix is to be kept
+  // --- radix select of the k-th largest key
   uint32_t prefix = 0, mask = 0;
   int krem = k;
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int i = tid; i < kSub * 256; i += NT) sub[i] = 0;
-    __syncthreads();
-    int* my = sub + (warp & (kSub - 1)) * 256;
-    for (int base = warp * 32; base < n; base += NT) {
-      const int i = base + lane;
-      const uint32_t key = i < n ? keys[i] : 0u;
-      const bool act = i < n && (key & mask) == prefix;
-      const uint32_t dig = act ? ((key >> shift) & 255u) : 256u;
-      const uint32_t same = __match_any_sync(0xffffffffu, dig);
-      if (act && lane == __ffs(same) - 1) atomicAdd(my + dig, __popc(same));
+    int* hp = hist + pass * kSelSub * 256;
+    if (pass > 0) {
+      int* my = hp + (warp & (kSelSub - 1)) * 256;
+      for (int base = warp * 32; base < n; base += NT) {
+        const int i = base + lane;
+        const uint32_t key = i < n ? keys[i] : 0u;
+        const bool act = i < n && (key & mask) == prefix;
+        const uint32_t dig = act ? ((key >> shift) & 255u) : 256u;
+        const uint32_t same = __match_any_sync(0xffffffffu, dig);
+        if (act && lane == __ffs(same) - 1) atomicAdd(my + dig, __popc(same));
+      }
+      __syncthreads();
     }
-    __syncthreads();
-    for (int i = tid; i < 256; i += NT) {
-      int t = 0;
-#pragma unroll
-      for (int j = 0; j < kSub; ++j) t += sub[j * 256 + i];
-      hist[i] = t;
-    }
-    __syncthreads();
     if (warp == 0) {
-      // lane L scans bins 255-8L .. 248-8L (descending)
+      // lane L scans bins 255-8L .. 248-8L (descending), summing the sub-histograms
       int cnt[8], tot = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        cnt[j] = hist[255 - 8 * lane - j];
-        tot += cnt[j];
+        const int bin = 255 - 8 * lane - j;
+        int c = 0;
+#pragma unroll
+        for (int sb = 0; sb < kSelSub; ++sb) c += hp[sb * 256 + bin];
+        cnt[j] = c;
+        tot += c;
       }
       int incl = tot;
 #pragma unroll
@@ -135,7 +161,7 @@ __device__ __forceinline__ void score_and_select(const Params& p, int b, const A
     prefix |= (uint32_t)scratch[0] << shift;
     mask |= 255u << shift;
     krem -= scratch[1];
-    if (krem == scratch[3]) break;   // all keys with this prefix are kept
+    if (krem == scratch[3]) break;   // every key with this prefix is kept
   }
   // keep: (key & mask) > prefix, or == prefix for the first krem such keys
   const uint32_t thr = prefix;
@@ -152,8 +178,8 @@ __device__ __forceinline__ void score_and_select(const Params& p, int b, const A
     gt += __popc(__ballot_sync(0xffffffffu, ok && key > thr));
     eq += __popc(__ballot_sync(0xffffffffu, ok && key == thr));
   }
-  int* s_gt = scratch + 4;
-  int* s_eq = scratch + 4 + NW;
+  int* s_gt = scratch + 8;
+  int* s_eq = scratch + 8 + NW;
   if (lane == 0) {
     s_gt[warp] = gt;
     s_eq[warp] = eq;
@@ -200,25 +226,7 @@ __device__ __forceinline__ void score_and_select(const Params& p, int b, const A
   }
 }
 
-constexpr int kSelectThreads = 1024;
-
-// Selection kernel of a focal layer: one CTA of 1024 threads per sequence,
-// launched right after the focal attend kernel (which left the per-KV-head
-// partial scores in the workspace).
-template <int NT>
-__global__ void __launch_bounds__(NT) select_kernel(const Params p) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  asm volatile("griddepcontrol.wait;\n" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  int bad = 0;  // already reported by the attend kernel
-  const AttendList L = make_list<kFocal>(p, blockIdx.x, bad);
-  score_and_select<NT>(p, blockIdx.x, L, smem);
-}
-
-inline int select_smem_bytes(int max_img) {
-  constexpr int NW = kSelectThreads / 32;
-  return TopkSmem::hist_offset(max_img) + 256 * 4 + 4 * 256 * 4 + (4 + 2 * NW) * 4 + NW * 8 + 16;
-}
+inline int select_smem_bytes(int max_img) { return SelectSmem::bytes(max_img); }
 
 inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, int smem, cudaStream_t stream,
                                      cudaLaunchAttribute* attr) {
@@ -446,19 +454,6 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
     }
   }
 
-  // The next kAhead tiles of every warp beyond the staged ones, and
-  // (speculatively) the selected image rows: pull them into L2 while waiting.
-  // Prefetches only warm the cache; the selection is read again after the wait.
-  {
-    const int u_end = min(n_txt0, kWarps * (kStages - 1 + kAhead) * kTile);
-    for (int u = kWarps * (kStages - 1) * kTile + tid; u < u_end; u += kThreads) {
-      const int row = srow[u];
-      if (row >= 0) {
-        prefetch_l2(kg + (size_t)row * D, ROWB);
-        prefetch_l2(vg + (size_t)row * D, ROWB);
-      }
-    }
-  }
   // Sparse: resolve this CTA's share of the selection speculatively from the
   // current k and idx (the previous kernel may still be writing them) and pull
   // those rows into L2. After the wait every thread re-reads its entries and
@@ -611,16 +606,6 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
     for (int it = 0; it < my_tiles; ++it) {
       if (it + kStages - 1 < my_tiles) issue(it + kStages - 1, n_round);
       cp_async_commit();
-      // keep this warp's tile kAhead beyond the pipeline on its way into L2
-      // (round 0 had its first kAhead such tiles prefetched before the wait)
-      {
-        const int ja = it + kStages - 1 + kAhead;
-        const int ua = (warp + ja * kWarps) * kTile + (lane & 15);
-        if (ja < my_tiles && ua < n_round) {
-          const int row = srow[ua];
-          if (row >= 0) prefetch_l2((lane < 16 ? kg : vg) + (size_t)row * D, ROWB);
-        }
-      }
       cp_async_wait<kStages - 1>();
       __syncwarp();
       const int stage = it % kStages;

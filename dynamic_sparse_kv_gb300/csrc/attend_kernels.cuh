@@ -36,7 +36,6 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 16;      // tokens per warp tile
 constexpr int kSlots = 8;      // query-head slots per KV head (g <= 8)
 constexpr int kStages = 3;     // cp.async pipeline depth per warp
-constexpr int kAhead = 4;      // tiles per warp kept in flight to L2 beyond the pipeline
 constexpr int kMaxSplits = 16;  // = the largest thread-block cluster used
 constexpr int kMaxImg = 16384; // image tokens whose scores fit in shared memory
 
@@ -262,12 +261,6 @@ struct EpiSmem {
   static constexpr int kInvL = kM + kSlots * 4;
   static constexpr int kScale = kInvL + kSlots * 4;
   static constexpr int kBytes = kScale + kMaxSplits * kSlots * 4;
-};
-
-struct TopkSmem {
-  // keys[max_img] (uint32), then hist[256] at a 16-byte boundary, then scan
-  // scratch (sized by the selection kernel)
-  __host__ __device__ static int hist_offset(int max_img) { return (max_img * 4 + 15) / 16 * 16; }
 };
 
 template <typename T, int D>
