@@ -25,7 +25,7 @@ FASTOCR_ERR_NO_DEVICE = -5
 FASTOCR_ERR_ALIGN = -6
 FASTOCR_DTYPE_F32 = 0
 FASTOCR_DTYPE_BF16 = 1
-DEV_BAD_PAGE, DEV_BAD_SEQLEN, DEV_BAD_IMG, DEV_BAD_SELECTION = 1, 2, 4, 8
+DEV_BAD_PAGE, DEV_BAD_SEQLEN, DEV_BAD_IMG, DEV_BAD_SELECTION, DEV_INTERNAL = 1, 2, 4, 8, 16
 
 
 class fastocr_dims(ctypes.Structure):

@@ -36,7 +36,7 @@ struct SelectSmem {
 // The selection is written in ascending position order.
 template <int NT>
 __global__ void __launch_bounds__(NT) select_kernel(const Params p) {
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem[];
   constexpr int NW = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.x;
@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(NT) select_kernel(const Params p) {
 
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  int bad = 0;  // already reported by the attend kernel
+  int bad = 0;  // make_list flags: already reported by the attend kernel
   const AttendList L = make_list<kFocal>(p, b, bad);
   const int n = L.n_img;
   __syncthreads();   // histograms zeroed
@@ -217,10 +217,17 @@ __global__ void __launch_bounds__(NT) select_kernel(const Params p) {
     const int my_eq_rank = eq_run + __popc(eq_b & lt_mask);
     const bool take = is_gt || (is_eq && my_eq_rank < krem);
     const uint32_t take_b = __ballot_sync(0xffffffffu, take);
-    if (take) dst[out_run + __popc(take_b & lt_mask)] = L.img_start + i;
+    const int slot = out_run + __popc(take_b & lt_mask);
+    if (take) {
+      if (slot < k)   // never false for a consistent selection; guards the store anyway
+        dst[slot] = L.img_start + i;
+      else
+        bad |= kDevInternal;
+    }
     eq_run += __popc(eq_b);
     out_run += __popc(take_b);
   }
+  if (bad & kDevInternal) atomicOr(p.status, kDevInternal);
 }
 
 inline int select_smem_bytes(int max_img) { return SelectSmem::bytes(max_img); }
@@ -244,13 +251,15 @@ inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, int smem, cudaStream
 //
 // Work list of one CTA. The mode's attend set minus the current token N_t-1
 // is the "text" list (at most two contiguous position ranges); the S CTAs of a
-// (sequence, KV head) take equal contiguous shares of it, the last CTA also
-// takes the current token, and in sparse mode every CTA takes an equal share
-// of the selection. Text entries -- cache rows of earlier tokens, their
-// pages, the lengths -- are final before the previous kernel on the stream
-// starts, so they are resolved and their first tiles staged into shared
-// memory before griddepcontrol.wait; the current token, the selection and q
-// are read only after it.
+// (sequence, KV head) take equal contiguous shares of it, in sparse mode every
+// CTA also takes an equal share of the selection, and the last CTA takes the
+// current token. Text entries -- cache rows of earlier tokens, their pages,
+// the lengths -- are final before the previous kernel on the stream starts,
+// so they are resolved and their first tiles staged into shared memory before
+// griddepcontrol.wait. So is the current token's row, but its K/V only after
+// the wait. The selection (k and idx) may be written by the previous kernel:
+// it is resolved and staged speculatively before the wait and checked after
+// it; q is read only after it.
 struct CtaList {
   int n_t;
   int a1, len1, a2, len2;   // text ranges [a1, a1+len1) and [a2, a2+len2)
@@ -357,11 +366,15 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
   int bad = 0;
   CtaList c = make_cta_list<MODE>(p, b, split, bad);
 
-  // cache position of work-list entry u (-1: masked)
-  // The text entries are padded to whole tiles (n_txt_pad), so that a tile
-  // never mixes text with late entries and every text tile can be staged
-  // before the wait; padding entries are masked.
+  // Work list of this CTA: [text, padded to whole tiles][selection, padded to
+  // whole tiles (sparse)][current token]. Padding entries are masked. A tile
+  // therefore never mixes entries of different kinds: text tiles and (in
+  // sparse mode, speculatively) selection tiles can be staged before the
+  // wait, and the current token, whose K/V the previous kernel may still be
+  // writing, sits alone in the last tile.
   const int n_txt_pad = (c.n_txt + kTile - 1) / kTile * kTile;
+  int n_sel_pad = 0;
+  // cache position of work-list entry u (-1: masked)
   auto pos_of = [&](int u) -> int {
     if (u < n_txt_pad) {
       if (u >= c.n_txt) return -1;
@@ -369,10 +382,8 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
       return t < c.len1 ? c.a1 + t : c.a2 + (t - c.len1);
     }
     u -= n_txt_pad;
-    if (c.has_cur) {
-      if (u == 0) return c.cur_pos;
-      u -= 1;
-    }
+    if (u >= n_sel_pad) return c.cur_pos;   // u == n_sel_pad, only with has_cur
+    if (u >= c.n_sel) return -1;
     const int pos = __ldcg(c.sel + c.sel_lo + u);
     if (pos < c.img_start || pos >= c.img_start + c.n_img) {
       bad |= kDevBadSelection;
@@ -412,65 +423,64 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
     }
   };
 
-  // Stage tile j of this warp in the current round: 2 x 16 rows in 16-byte
-  // chunks, each instruction covering whole rows.
+  // Stage tile j of this warp in the current round: 16 K rows and 16 V rows
+  // in 16-byte chunks. One instruction covers 32/CH whole rows; a lane takes
+  // chunk `lane % CH` of rows `lane / CH`, `lane / CH + 32/CH`, ..., and reads
+  // each row index once for both K and V. Masked rows are zero-filled.
+  static_assert(CH <= 32 && 32 % CH == 0, "a row must fit one warp instruction");
+  const int n_rows = (p.num_pages * p.Hkv) << p.log2_page;   // < 2^31, checked on the host
+  constexpr int kRowsPerInst = 32 / CH;
+  const int ch_lane = lane % CH, row_lane = lane / CH;
   auto issue = [&](int j, int n_round) {
     const int stage = j % kStages;
     const int base = (warp + j * kWarps) * kTile;
-    long long rowoff = -1;
-    if (lane < kTile && base + lane < n_round) {
-      const int row = srow[base + lane];
-      rowoff = row >= 0 ? (long long)row * D : -1;
-    }
     const uint32_t sb = smem_u32(pipe + stage * SM::kStageBytes);
+    int rows[kTile / kRowsPerInst];
 #pragma unroll
-    for (int i = 0; i < 2 * kTile * CH / 32; ++i) {
-      const int cc = i * 32 + lane;
-      const int kv = cc / (kTile * CH);
-      const int rem = cc % (kTile * CH);
-      const int row = rem / CH, ch = rem % CH;
-      const long long ro = __shfl_sync(0xffffffffu, rowoff, row);
-      const T* src = (kv == 0 ? kg : vg) + (ro < 0 ? 0 : ro) + ch * kElemPerChunk;
-      const uint32_t dst = sb + kv * (kTile * ROWB) + row * ROWB + ((ch ^ (row & 7)) << 4);
-      cp_async16(dst, src, ro < 0 ? 0 : 16);
+    for (int i = 0; i < kTile / kRowsPerInst; ++i) {
+      const int r = i * kRowsPerInst + row_lane;
+      rows[i] = base + r < n_round ? srow[base + r] : -1;
+      if (rows[i] >= n_rows) {   // never true for a resolved row; guards the copy anyway
+        bad |= kDevInternal;
+        rows[i] = -1;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kTile / kRowsPerInst; ++i) {
+      const int r = i * kRowsPerInst + row_lane;
+      const size_t off = (size_t)max(rows[i], 0) * D + ch_lane * kElemPerChunk;
+      const int bytes = rows[i] >= 0 ? 16 : 0;
+      const uint32_t dst = sb + r * ROWB + ((ch_lane ^ (r & 7)) << 4);
+      cp_async16(dst, kg + off, bytes);
+      cp_async16(dst + kTile * ROWB, vg + off, bytes);
     }
   };
 
-  // ---------------- before the previous kernel completes: text entries of round 0
+  // ---------------- before the previous kernel completes
+  // Rows of round 0: the text, the selection (sparse; speculative, since the
+  // previous kernel may still be writing k and idx) and the current token
+  // (its row is final now, its K/V may not be). Then every whole tile of this
+  // warp that the pipeline holds, up to but excluding the current token's.
+  constexpr int kPer = kSliceMax / kThreads;
   const int n_txt0 = min(n_txt_pad, kSliceMax);
   resolve(0, 0, n_txt0);
-  __syncthreads();
-  int pre_issued = 0;   // leading tiles of this warp already staged
-#pragma unroll
-  for (int j = 0; j < kStages - 1; ++j) {
-    const int end = (warp + j * kWarps + 1) * kTile;   // tile must hold text entries only
-    if (pre_issued == j && end <= n_txt0) {
-      issue(j, n_txt0);
-      cp_async_commit();
-      ++pre_issued;
-    }
-  }
-
-  // Sparse: resolve this CTA's share of the selection speculatively from the
-  // current k and idx (the previous kernel may still be writing them) and pull
-  // those rows into L2. After the wait every thread re-reads its entries and
-  // the CTA keeps the speculative rows only if nothing changed.
-  constexpr int kPer = kSliceMax / kThreads;
-  const int sel_u0 = n_txt_pad + c.has_cur;   // first selection entry of the work list
-  int spec_k = -1, spec_lo = 0, spec_u1 = sel_u0;
+  int spec_u1 = n_txt_pad;   // speculative selection entries: [n_txt_pad, spec_u1)
   int spec_raw[kPer];
   if (MODE == kSparse) {
     const int k_cap = min(c.n_img, p.idx_stride);
-    spec_k = min(max(__ldcg(p.k_in + b), 0), k_cap);
+    const int spec_k = min(max(__ldcg(p.k_in + b), 0), k_cap);
     const int per = (spec_k + p.splits - 1) / p.splits;
-    spec_lo = split * per;
-    const int n_sel = max(0, min(per, spec_k - spec_lo));
-    spec_u1 = min(kSliceMax, sel_u0 + n_sel);
+    c.sel_lo = split * per;
+    c.n_sel = max(0, min(per, spec_k - c.sel_lo));
+    n_sel_pad = (c.n_sel + kTile - 1) / kTile * kTile;
+    spec_u1 = min(kSliceMax, n_txt_pad + c.n_sel);
+    const int u_pad = min(kSliceMax, n_txt_pad + n_sel_pad);
+    const int u_staged = kWarps * kStages * kTile;   // entries the pre-wait tiles can cover
     int pos[kPer], page[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-      const int u = sel_u0 + tid + j * kThreads;
-      spec_raw[j] = u < spec_u1 ? __ldcg(c.sel + spec_lo + (u - sel_u0)) : -1;
+      const int u = n_txt_pad + tid + j * kThreads;
+      spec_raw[j] = u < spec_u1 ? __ldcg(c.sel + c.sel_lo + (u - n_txt_pad)) : -1;
       pos[j] = (u < spec_u1 && spec_raw[j] >= c.img_start && spec_raw[j] < c.img_start + c.n_img)
                    ? spec_raw[j] : -1;
     }
@@ -478,13 +488,15 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
     for (int j = 0; j < kPer; ++j) page[j] = pos[j] >= 0 ? __ldcg(bt + (pos[j] >> p.log2_page)) : -1;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-      const int u = sel_u0 + tid + j * kThreads;
-      if (u >= spec_u1) continue;
+      const int u = n_txt_pad + tid + j * kThreads;
+      if (u >= u_pad) continue;
       int row = -1, ps = pos[j];
       if (ps >= 0 && page[j] >= 0 && page[j] < p.num_pages) {
         row = ((page[j] * p.Hkv + hkv) << p.log2_page) | (ps & page_mask);
-        prefetch_l2(kg + (size_t)row * D, ROWB);
-        prefetch_l2(vg + (size_t)row * D, ROWB);
+        if (u >= u_staged) {   // beyond the staged tiles: pull into L2 for later
+          prefetch_l2(kg + (size_t)row * D, ROWB);
+          prefetch_l2(vg + (size_t)row * D, ROWB);
+        }
       } else {
         ps = -1;
       }
@@ -492,11 +504,46 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
       spos[u] = ps;
     }
   }
+  const int n_pre = min(kSliceMax, n_txt_pad + n_sel_pad);   // entries before the current token
+  if (c.has_cur && tid == 0 && n_pre < kSliceMax) {
+    const int page = __ldcg(bt + (c.cur_pos >> p.log2_page));
+    int row = -1, ps = c.cur_pos;
+    if (page >= 0 && page < p.num_pages) {
+      row = ((page * p.Hkv + hkv) << p.log2_page) | (ps & page_mask);
+    } else {
+      bad |= kDevBadPage;
+      ps = -1;
+    }
+    srow[n_pre] = row;
+    spos[n_pre] = ps;
+  }
+  __syncthreads();
+  int pre_issued = 0;   // leading tiles of this warp already staged
+#pragma unroll
+  for (int j = 0; j < kStages; ++j) {
+    const int end = (warp + j * kWarps + 1) * kTile;
+    if (pre_issued == j && end <= n_pre) {
+      issue(j, n_pre);
+      cp_async_commit();
+      ++pre_issued;
+    }
+  }
 
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   if (p.pdl_early) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
-  // ---------------- after it: q, selection, current token (loads issued together)
+  // ---------------- after it: the current token's tile, q and the final
+  // selection, all in flight together. The tile follows the staged ones in
+  // its warp's order (sparse: under the speculative layout, redone below if
+  // the speculation fails).
+  if (c.has_cur && n_pre < kSliceMax) {
+    const int t_cur = n_pre / kTile;   // n_pre is a multiple of kTile here
+    if (warp == t_cur % kWarps && pre_issued == t_cur / kWarps && pre_issued < kStages) {
+      issue(pre_issued, n_pre + 1);
+      cp_async_commit();
+      ++pre_issued;
+    }
+  }
   WarpStateMma<D> sm_;
   WarpStateF32<D> sf_;
   const int gid = lane >> 2, tig = lane & 3;
@@ -509,51 +556,41 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
       sm_.qf[ks][1] = have ? __ldcg(reinterpret_cast<const unsigned int*>(qrow + 16 * ks + 8 + 2 * tig)) : 0u;
     }
   }
-  int cur_page = -1;
-  if (c.has_cur && tid == 0 && n_txt_pad < kSliceMax) cur_page = __ldcg(bt + (c.cur_pos >> p.log2_page));
-  bool keep_spec = true;
   if (MODE == kSparse) {
+    // keep the speculative entries only if this CTA's share is unchanged
     const int k = __ldcg(p.k_in + b);
     int raw2[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-      const int u = sel_u0 + tid + j * kThreads;
-      raw2[j] = u < spec_u1 ? __ldcg(c.sel + spec_lo + (u - sel_u0)) : -1;
+      const int u = n_txt_pad + tid + j * kThreads;
+      raw2[j] = u < spec_u1 ? __ldcg(c.sel + c.sel_lo + (u - n_txt_pad)) : -1;
     }
+    const int spec_lo = c.sel_lo, spec_n = c.n_sel;
     add_selection(p, k, split, c, bad);
-    int ok = c.sel_lo == spec_lo && min(kSliceMax, sel_u0 + c.n_sel) == spec_u1;
+    int ok = c.sel_lo == spec_lo && c.n_sel == spec_n;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-      const int u = sel_u0 + tid + j * kThreads;
+      const int u = n_txt_pad + tid + j * kThreads;
       if (u < spec_u1 && raw2[j] != spec_raw[j]) ok = 0;
     }
-    keep_spec = __syncthreads_and(ok) != 0;
-    if (keep_spec) {   // the speculative entries are the real ones: report the faulty ones
+    if (__syncthreads_and(ok)) {   // the speculative entries are the real ones: report faulty ones
 #pragma unroll
       for (int j = 0; j < kPer; ++j) {
-        const int u = sel_u0 + tid + j * kThreads;
+        const int u = n_txt_pad + tid + j * kThreads;
         if (u >= spec_u1) continue;
         if (raw2[j] < c.img_start || raw2[j] >= c.img_start + c.n_img)
           bad |= kDevBadSelection;
         else if (spos[u] < 0)
           bad |= kDevBadPage;
       }
+    } else {   // drop the staged tiles and lay out the selection and current token again
+      cp_async_wait<0>();
+      pre_issued = 0;
+      n_sel_pad = (c.n_sel + kTile - 1) / kTile * kTile;
+      resolve(0, n_txt_pad, min(n_txt_pad + n_sel_pad + c.has_cur, kSliceMax));
     }
   }
-  if (cur_page >= 0 || (c.has_cur && tid == 0 && n_txt_pad < kSliceMax)) {
-    int row = -1, ps = c.cur_pos;
-    if (cur_page >= 0 && cur_page < p.num_pages) {
-      row = ((cur_page * p.Hkv + hkv) << p.log2_page) | (ps & page_mask);
-    } else {
-      bad |= kDevBadPage;
-      ps = -1;
-    }
-    srow[n_txt_pad] = row;
-    spos[n_txt_pad] = ps;
-  }
-  const int n_cta = n_txt_pad + c.has_cur + c.n_sel;
-  const int n_round0 = min(n_cta, kSliceMax);
-  if (!keep_spec && n_round0 > sel_u0) resolve(0, sel_u0, n_round0);
+  const int n_cta = n_txt_pad + n_sel_pad + c.has_cur;
 
   float* logit_base = nullptr;
   if (MODE == kFocal)
@@ -601,7 +638,8 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
       cp_async_commit();
     }
     for (int it = 0; it < my_tiles; ++it) {
-      if (it + kStages - 1 < my_tiles) issue(it + kStages - 1, n_round);
+      const int jn = it + kStages - 1;   // tiles below `first` were staged already
+      if (jn >= first && jn < my_tiles) issue(jn, n_round);
       cp_async_commit();
       cp_async_wait<kStages - 1>();
       __syncwarp();
@@ -611,10 +649,13 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
       const int tbase = (warp + it * kWarps) * kTile;   // tile start within the round
 
       if constexpr (kMma) {
-        // S^T[16 keys x 8 heads] = K[16 x D] . Q^T[D x 8], two independent
-        // accumulation chains (even / odd 16-wide slices of d) to halve the
-        // dependent MMA latency
-        float ce[4] = {0.f, 0.f, 0.f, 0.f}, co[4] = {0.f, 0.f, 0.f, 0.f};
+        // S^T[16 keys x 8 heads] = K[16 x D] . Q^T[D x 8] in kChains independent
+        // accumulation chains (16-wide slices of d taken round robin) to cut
+        // the dependent MMA latency
+        constexpr int kChains = D / 16 >= 4 ? 4 : D / 16;
+        float cc[kChains][4];
+#pragma unroll
+        for (int q = 0; q < kChains; ++q) cc[q][0] = cc[q][1] = cc[q][2] = cc[q][3] = 0.f;
         const uint32_t kA = smem_u32(kS), vA = smem_u32(vS);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
@@ -622,9 +663,16 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
           const int ch = 2 * ks + (lane >> 4);
           uint32_t a[4];
           ldmatrix_x4(a, kA + row * ROWB + ((ch ^ (row & 7)) << 4));
-          mma_bf16((ks & 1) ? co : ce, a, sm_.qf[ks][0], sm_.qf[ks][1]);
+          mma_bf16(cc[ks % kChains], a, sm_.qf[ks][0], sm_.qf[ks][1]);
         }
-        const float cfr[4] = {ce[0] + co[0], ce[1] + co[1], ce[2] + co[2], ce[3] + co[3]};
+        float cfr[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float s = cc[0][e];
+#pragma unroll
+          for (int q = 1; q < kChains; ++q) s += cc[q][e];
+          cfr[e] = s;
+        }
         // cache positions of keys gid and gid+8 (-1: masked or past the end)
         const int posA = tbase + gid < n_round ? spos[tbase + gid] : -1;
         const int posB = tbase + gid + 8 < n_round ? spos[tbase + gid + 8] : -1;
@@ -640,26 +688,40 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
             *reinterpret_cast<float2*>(logit_base + (size_t)(posB - c.img_start) * kSlots + 2 * tig) =
                 make_float2(s2, s3);
         }
-        const float mx0 = warp_max_gid(fmaxf(s0, s2));
-        const float mx1 = warp_max_gid(fmaxf(s1, s3));
-        const float mn0 = fmaxf(sm_.m[0], mx0), mn1 = fmaxf(sm_.m[1], mx1);
-        const float b0f = mn0 == kNegInf ? 0.f : mn0, b1f = mn1 == kNegInf ? 0.f : mn1;
-        const float al0 = fast_exp2(sm_.m[0] - b0f), al1 = fast_exp2(sm_.m[1] - b1f);
+        // Online softmax with a lazily moved running max (base-2 logits): the
+        // max and the output scale are updated only when a score exceeds the
+        // running max by more than kLazyMax, so most tiles need neither the
+        // cross-lane max nor a rescale; probabilities stay below 2^kLazyMax.
+        if (__any_sync(0xffffffffu, s0 > sm_.m[0] + kLazyMax || s2 > sm_.m[0] + kLazyMax ||
+                                        s1 > sm_.m[1] + kLazyMax || s3 > sm_.m[1] + kLazyMax)) {
+          const float mx0 = warp_max_gid(fmaxf(s0, s2));
+          const float mx1 = warp_max_gid(fmaxf(s1, s3));
+          const float mn0 = fmaxf(sm_.m[0], mx0), mn1 = fmaxf(sm_.m[1], mx1);
+          const float al0 = fast_exp2(sm_.m[0] - (mn0 == kNegInf ? 0.f : mn0));
+          const float al1 = fast_exp2(sm_.m[1] - (mn1 == kNegInf ? 0.f : mn1));
+          sm_.l[0] *= al0;
+          sm_.l[1] *= al1;
+          sm_.m[0] = mn0;
+          sm_.m[1] = mn1;
+#pragma unroll
+          for (int mt = 0; mt < D / 16; ++mt) {
+            sm_.acc[mt][0] *= al0;
+            sm_.acc[mt][1] *= al1;
+            sm_.acc[mt][2] *= al0;
+            sm_.acc[mt][3] *= al1;
+          }
+        }
+        const float b0f = sm_.m[0] == kNegInf ? 0.f : sm_.m[0];
+        const float b1f = sm_.m[1] == kNegInf ? 0.f : sm_.m[1];
         const float p0 = fast_exp2(s0 - b0f), p2 = fast_exp2(s2 - b0f);
         const float p1 = fast_exp2(s1 - b1f), p3 = fast_exp2(s3 - b1f);
-        sm_.l[0] = sm_.l[0] * al0 + (p0 + p2);
-        sm_.l[1] = sm_.l[1] * al1 + (p1 + p3);
-        sm_.m[0] = mn0;
-        sm_.m[1] = mn1;
+        sm_.l[0] += p0 + p2;
+        sm_.l[1] += p1 + p3;
         // P^T[16 keys x 8 heads] as the B operand: transpose the two 8x8 blocks
         const uint32_t bb0 = movmatrix_trans(pack_bf16(p0, p1));
         const uint32_t bb1 = movmatrix_trans(pack_bf16(p2, p3));
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
-          sm_.acc[mt][0] *= al0;
-          sm_.acc[mt][1] *= al1;
-          sm_.acc[mt][2] *= al0;
-          sm_.acc[mt][3] *= al1;
           const int row = (lane & 7) + ((lane >> 4) << 3);
           const int ch = 2 * mt + ((lane >> 3) & 1);
           uint32_t a[4];
@@ -778,32 +840,12 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
   if (bad) atomicOr(p.status, bad);
   __syncthreads();
 
-  // ---------------- CTA partial per head: max, sum, per-warp scales
-  float* cm = reinterpret_cast<float*>(smem + E::kCtaM);     // [8]
-  float* cl = reinterpret_cast<float*>(smem + E::kCtaL);     // [8]
-  float* csc = reinterpret_cast<float*>(smem + E::kCtaSc);   // [W][8]
-  if (tid < kSlots) {
-    const int h = tid;
-    float M = kNegInf;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * kSlots + h]);
-    const float base = M == kNegInf ? 0.f : M;
-    float Ls = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float sc = fast_exp2(wm[w * kSlots + h] - base);
-      csc[w * kSlots + h] = sc;
-      Ls = fmaf(wl[w * kSlots + h], sc, Ls);
-    }
-    cm[h] = M;
-    cl[h] = Ls;
-  }
-  __syncthreads();
-
-  // ---------------- push the partial to the CTAs of the cluster
+  // ---------------- push the CTA partial to the CTAs of the cluster
   // CTA `r` of the S splits owns output pairs [r*per, (r+1)*per) of the
   // (head, 4 dims) pairs; every CTA writes its share of each owner's pairs,
   // and its per-head (max, sum), straight into the owner's shared memory.
+  // The CTA partial (its W warps merged) is formed by the pushing threads
+  // themselves: a thread needs only its head's W (max, sum) pairs.
   const int S = p.splits;
   const uint32_t rank = cluster_ctarank();
   constexpr int C4 = D / 4;
@@ -811,23 +853,38 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
   const int per = (n_pairs + S - 1) / S;
   float* rml = reinterpret_cast<float*>(smem + SM::kRecvMl);     // [S][8][2]
   float* racc = reinterpret_cast<float*>(smem + SM::kRecvAcc);   // [S][per][4]
+  auto warp_scales = [&](int h, float sc[kWarps]) -> float {   // CTA max of head h
+    float M = kNegInf;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * kSlots + h]);
+    const float base = M == kNegInf ? 0.f : M;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) sc[w] = fast_exp2(wm[w * kSlots + h] - base);
+    return M;
+  };
   cluster_wait();   // every CTA of the cluster has started (its receive area exists)
   if (MODE == kFocal) __threadfence();   // logits of this CTA, read by others below
   for (int e = tid; e < S * kSlots; e += kThreads) {
     const int r = e / kSlots, h = e % kSlots;
-    st_dsmem_f32x2(rml + (rank * kSlots + h) * 2, r, cm[h], cl[h]);
+    float sc[kWarps];
+    const float M = warp_scales(h, sc);
+    float L = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) L = fmaf(wl[w * kSlots + h], sc[w], L);
+    st_dsmem_f32x2(rml + (rank * kSlots + h) * 2, r, M, L);
   }
   for (int e = tid; e < n_pairs; e += kThreads) {
     const int h = e / C4, c4 = e % C4;
+    float sc[kWarps];
+    warp_scales(h, sc);
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      const float sc = csc[w * kSlots + h];
       const float4 v = *reinterpret_cast<const float4*>(wacc + (w * kSlots + h) * D + 4 * c4);
-      a.x = fmaf(v.x, sc, a.x);
-      a.y = fmaf(v.y, sc, a.y);
-      a.z = fmaf(v.z, sc, a.z);
-      a.w = fmaf(v.w, sc, a.w);
+      a.x = fmaf(v.x, sc[w], a.x);
+      a.y = fmaf(v.y, sc[w], a.y);
+      a.z = fmaf(v.z, sc[w], a.z);
+      a.w = fmaf(v.w, sc[w], a.w);
     }
     const int r = e / per;
     st_dsmem_f32x4(racc + ((size_t)rank * per + (e - r * per)) * 4, r, a);
@@ -835,30 +892,17 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
   cluster_sync();   // release the pushes, acquire everyone else's
 
   // ---------------- owner: merge the S partials of its pairs (local memory only)
-  float* sM = reinterpret_cast<float*>(smem + E::kM);
-  float* sInvL = reinterpret_cast<float*>(smem + E::kInvL);
-  float* sScale = reinterpret_cast<float*>(smem + E::kScale);   // [S][8]
-  // per-head max and sum over the S partials: warp w takes heads w and w+4,
-  // lane s reads partial s
-  for (int h = warp; h < kSlots; h += kWarps) {
-    const float ms = lane < S ? rml[(lane * kSlots + h) * 2] : kNegInf;
-    const float ls = lane < S ? rml[(lane * kSlots + h) * 2 + 1] : 0.f;
-    float M = ms;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    const float base = M == kNegInf ? 0.f : M;
-    const float sc = lane < S ? fast_exp2(ms - base) : 0.f;
-    float Ls = ls * sc;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
-    const float inv = Ls > 0.f ? __frcp_rn(Ls) : 0.f;
-    if (lane < S) sScale[lane * kSlots + h] = sc * inv;
-    if (lane == 0) {
-      sM[h] = base;
-      sInvL[h] = inv;
-    }
-  }
-  __syncthreads();
+  // Each thread forms its head's max and 1/sum over the S partials itself
+  // (broadcast reads), so the merge needs no further barrier.
+  auto head_stats = [&](int h, float& base, float& inv) {
+    float M = kNegInf;
+    for (int s = 0; s < S; ++s) M = fmaxf(M, rml[(s * kSlots + h) * 2]);
+    base = M == kNegInf ? 0.f : M;
+    float L = 0.f;
+    for (int s = 0; s < S; ++s)
+      L = fmaf(rml[(s * kSlots + h) * 2 + 1], fast_exp2(rml[(s * kSlots + h) * 2] - base), L);
+    inv = L > 0.f ? __frcp_rn(L) : 0.f;
+  };
   {
     // G adjacent lanes share one output pair, each summing every G-th partial
     T* outp = static_cast<T*>(p.out) + ((size_t)b * p.Hq + (size_t)hkv * p.g) * D;
@@ -873,9 +917,11 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
       const bool ok = e < e_hi;
       const int h = ok ? e / C4 : 0, c4 = ok ? e % C4 : 0;
       if (ok) {
+        float base, inv;
+        head_stats(h, base, inv);
         for (int s = sub; s < S; s += G) {
           const float4 v = *reinterpret_cast<const float4*>(racc + ((size_t)s * per + (e - e_lo)) * 4);
-          const float sc = sScale[s * kSlots + h];
+          const float sc = fast_exp2(rml[(s * kSlots + h) * 2] - base) * inv;
           acc.x = fmaf(v.x, sc, acc.x);
           acc.y = fmaf(v.y, sc, acc.y);
           acc.z = fmaf(v.z, sc, acc.z);
@@ -904,6 +950,10 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
 
   // ---------------- focal: this group's share of the image scores, split over the cluster
   if constexpr (MODE == kFocal) {
+    float* sM = reinterpret_cast<float*>(smem + E::kM);
+    float* sInvL = reinterpret_cast<float*>(smem + E::kInvL);
+    if (tid < kSlots) head_stats(tid, sM[tid], sInvL[tid]);
+    __syncthreads();
     float Mh[kSlots], iL[kSlots];
 #pragma unroll
     for (int h = 0; h < kSlots; ++h) {

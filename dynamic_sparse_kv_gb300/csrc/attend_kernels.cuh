@@ -36,6 +36,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 16;      // tokens per warp tile
 constexpr int kSlots = 8;      // query-head slots per KV head (g <= 8)
 constexpr int kStages = 3;     // cp.async pipeline depth per warp
+constexpr float kLazyMax = 8.f; // running-max slack (log2 units) before a rescale
 constexpr int kMaxSplits = 16;  // = the largest thread-block cluster used
 constexpr int kMaxImg = 16384; // image tokens whose scores fit in shared memory
 
@@ -46,6 +47,7 @@ constexpr int kDevBadPage = 1;
 constexpr int kDevBadSeqLen = 2;
 constexpr int kDevBadImg = 4;
 constexpr int kDevBadSelection = 8;
+constexpr int kDevInternal = 16;   // a cache row outside the cache reached a copy
 
 struct Params {
   const void* q;
@@ -108,13 +110,15 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t r[4], uint32_t addr) 
 }
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
   return y;
 }
-// D(16x8, f32) += A(16x16, bf16, row) * B(16x8, bf16, col)
+// D(16x8, f32) += A(16x16, bf16, row) * B(16x8, bf16, col). Register-only
+// operations (this and movmatrix) are left free for the compiler to schedule;
+// ldmatrix stays ordered after the cp.async waits.
 __device__ __forceinline__ void mma_bf16(float c[4], const uint32_t a[4], uint32_t b0,
                                          uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
       "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
@@ -249,18 +253,13 @@ struct Smem {
 template <int D>
 struct EpiSmem {
   // reuses the pipeline area once streaming is done: per-warp partials
-  // wm[W][8], wl[W][8], wacc[W][8][D]; CTA max/sum/warp scales; the owner's
-  // merge scratch M[8], invL[8], scale[kMaxSplits][8]
+  // wm[W][8], wl[W][8], wacc[W][8][D]; focal: the heads' max M[8], 1/sum invL[8]
   static constexpr int kWm = 0;
   static constexpr int kWl = kWm + kWarps * kSlots * 4;
   static constexpr int kWacc = kWl + kWarps * kSlots * 4;
-  static constexpr int kCtaM = kWacc + kWarps * kSlots * D * 4;
-  static constexpr int kCtaL = kCtaM + kSlots * 4;
-  static constexpr int kCtaSc = kCtaL + kSlots * 4;
-  static constexpr int kM = kCtaSc + kWarps * kSlots * 4;
+  static constexpr int kM = kWacc + kWarps * kSlots * D * 4;
   static constexpr int kInvL = kM + kSlots * 4;
-  static constexpr int kScale = kInvL + kSlots * 4;
-  static constexpr int kBytes = kScale + kMaxSplits * kSlots * 4;
+  static constexpr int kBytes = kInvL + kSlots * 4;
 };
 
 template <typename T, int D>

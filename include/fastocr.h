@@ -95,6 +95,7 @@ typedef enum { FASTOCR_DTYPE_F32 = 0, FASTOCR_DTYPE_BF16 = 1 } fastocr_dtype;
 #define FASTOCR_DEV_BAD_SEQLEN 2    /* seq_len < 1 or above max_pages_per_seq*page_size */
 #define FASTOCR_DEV_BAD_IMG 4       /* img_range outside [0, N_t) */
 #define FASTOCR_DEV_BAD_SELECTION 8 /* selected position outside the image, or k > N_img */
+#define FASTOCR_DEV_INTERNAL 16     /* a kernel-internal consistency check failed (a library bug) */
 
 /* Shapes fixed for the life of a handle. */
 typedef struct {

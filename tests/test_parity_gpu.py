@@ -146,6 +146,52 @@ def test_constant_keys_ties_to_lowest():
         assert_close(out[b], ref, TOL["bf16"])
 
 
+@pytest.mark.parametrize("pattern", ["peaked", "rising"])
+def test_large_and_rising_logits(pattern):
+    """Logits far apart (a near one-hot softmax) or rising along the cache (the
+    running max moves again and again): full, focal and sparse outputs and the
+    focal selection still match the oracle."""
+    from dynamic_sparse_kv_gb300 import _native as N
+    case = _case("qwen7b_b1", batch=2, layers=1, prompt=37, grid=(1, 24, 20), steps=40, tau=0.1)
+    wl = case.wl
+    n_t = wl.seq_len_at(39)
+    q = case.q_at(39)[0].contiguous()
+    if pattern == "peaked":
+        q.mul_(12.0)
+    else:   # scale every cached key by a factor growing with its position
+        bt = case.block_table.long()
+        pos = torch.arange(bt.shape[1] * wl.page_size, device="cuda", dtype=torch.float32)
+        grow = (1.0 + 4.0 * pos / wl.max_tokens).to(case.k_cache.dtype)
+        for b in range(wl.batch):
+            for blk in range(bt.shape[1]):
+                page = int(bt[b, blk])
+                g = grow[blk * wl.page_size:(blk + 1) * wl.page_size]
+                case.k_cache[0, page] *= g.view(1, -1, 1)
+    dec = _direct(case, n_t)
+    out_full, out_focal, out_sparse = (torch.empty_like(q) for _ in range(3))
+    idx = torch.zeros(wl.batch, dec.stride, dtype=torch.int32, device="cuda")
+    k = torch.zeros(wl.batch, dtype=torch.int32, device="cuda")
+    N.fastocr_full_attend(dec.handle, q, dec.kv[0], out_full)
+    N.fastocr_focal_attend(dec.handle, q, dec.kv[0], case.img_range, wl.tau, out_focal, idx,
+                           dec.stride, k)
+    N.fastocr_sparse_attend(dec.handle, q, dec.kv[0], case.img_range, idx, dec.stride, k,
+                            out_sparse)
+    torch.cuda.synchronize()
+    assert dec.device_status() == 0
+    kv = KVCache(case)
+    for b in range(wl.batch):
+        Kl, Vl = kv(0, b)
+        qb = np64(q[b])
+        assert_close(out_full[b], A.full_attend(qb, Kl, Vl, n_t), TOL["bf16"], f"full b={b}")
+        ref_out, ref_sel, sigma = A.focal_attend(qb, Kl, Vl, n_t, wl.prompt, wl.n_img, wl.tau)
+        assert_close(out_focal[b], ref_out, TOL["bf16"], f"focal b={b}")
+        kk = int(k[b])
+        got = idx[b, :kk].cpu().numpy()
+        check_selection(got, ref_sel, sigma, wl.prompt, f"focal b={b}")
+        ref_sp = A.sparse_attend(qb, Kl, Vl, n_t, wl.prompt, wl.n_img, got)
+        assert_close(out_sparse[b], ref_sp, TOL["bf16"], f"sparse b={b}")
+
+
 def test_sparse_selection_permutation_and_empty():
     """Gather order does not matter; an empty attend list gives zeros."""
     from dynamic_sparse_kv_gb300 import _native as N
