@@ -45,13 +45,16 @@ __global__ void __launch_bounds__(NT) select_kernel(const Params p) {
   int* scratch = reinterpret_cast<int*>(smem + SelectSmem::scratch_offset(p.max_img));
   double* dscr = reinterpret_cast<double*>(scratch + 8 + 2 * NW);
   for (int i = tid; i < 4 * kSelSub * 256; i += NT) hist[i] = 0;
-
-  asm volatile("griddepcontrol.wait;\n" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  // lengths and image range are final before the attend kernel starts, so
+  // the keep count (double arithmetic, one thread) is known before the wait
   int bad = 0;  // make_list flags: already reported by the attend kernel
   const AttendList L = make_list<kFocal>(p, b, bad);
   const int n = L.n_img;
-  __syncthreads();   // histograms zeroed
+  if (tid == NT - 1) scratch[2] = keep_count(p.tau, n);
+
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  __syncthreads();   // histograms zeroed, keep count known
 
   // keys = sum of the KV heads' shares (fixed order); first-pass histogram
   const bool profiling = p.profile_layer >= 0;
@@ -92,11 +95,7 @@ __global__ void __launch_bounds__(NT) select_kernel(const Params p) {
     for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
     if (lane == 0) dscr[warp] = local;
   }
-  if (tid == 0) {
-    const int k = keep_count(p.tau, n);   // double arithmetic: one thread only
-    scratch[2] = k;
-    p.k_out[b] = k;
-  }
+  if (tid == 0) p.k_out[b] = scratch[2];
   __syncthreads();
   if (profiling && tid == 0) {
     double tot = 0.0;
@@ -467,8 +466,14 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
   int spec_u1 = n_txt_pad;   // speculative selection entries: [n_txt_pad, spec_u1)
   int spec_raw[kPer];
   if (MODE == kSparse) {
+    // One thread reads k and the CTA shares that reading: the previous kernel
+    // may be writing k, and threads that saw different values would lay out
+    // (and stage) the list differently.
+    int* s_spec_k = reinterpret_cast<int*>(smem + SM::kSpecK);
+    if (tid == 0) *s_spec_k = __ldcg(p.k_in + b);
+    __syncthreads();
     const int k_cap = min(c.n_img, p.idx_stride);
-    const int spec_k = min(max(__ldcg(p.k_in + b), 0), k_cap);
+    const int spec_k = min(max(*s_spec_k, 0), k_cap);
     const int per = (spec_k + p.splits - 1) / p.splits;
     c.sel_lo = split * per;
     c.n_sel = max(0, min(per, spec_k - c.sel_lo));
@@ -863,7 +868,6 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
     return M;
   };
   cluster_wait();   // every CTA of the cluster has started (its receive area exists)
-  if (MODE == kFocal) __threadfence();   // logits of this CTA, read by others below
   for (int e = tid; e < S * kSlots; e += kThreads) {
     const int r = e / kSlots, h = e % kSlots;
     float sc[kWarps];
@@ -895,12 +899,19 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
   // Each thread forms its head's max and 1/sum over the S partials itself
   // (broadcast reads), so the merge needs no further barrier.
   auto head_stats = [&](int h, float& base, float& inv) {
+    float ms[kMaxSplits], ls[kMaxSplits];   // all reads issued together
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) {
+      ms[s] = s < S ? rml[(s * kSlots + h) * 2] : kNegInf;
+      ls[s] = s < S ? rml[(s * kSlots + h) * 2 + 1] : 0.f;
+    }
     float M = kNegInf;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, rml[(s * kSlots + h) * 2]);
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) M = fmaxf(M, ms[s]);
     base = M == kNegInf ? 0.f : M;
     float L = 0.f;
-    for (int s = 0; s < S; ++s)
-      L = fmaf(rml[(s * kSlots + h) * 2 + 1], fast_exp2(rml[(s * kSlots + h) * 2] - base), L);
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) L = fmaf(ls[s], fast_exp2(ms[s] - base), L);
     inv = L > 0.f ? __frcp_rn(L) : 0.f;
   };
   {
@@ -948,7 +959,9 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
     }
   }
 
-  // ---------------- focal: this group's share of the image scores, split over the cluster
+  // ---------------- focal: scores of the image tokens this CTA streamed
+  // (its text share; the last CTA also the current token) from the logits it
+  // wrote itself and the heads' final max and sum: no other CTA's writes read
   if constexpr (MODE == kFocal) {
     float* sM = reinterpret_cast<float*>(smem + E::kM);
     float* sInvL = reinterpret_cast<float*>(smem + E::kInvL);
@@ -960,10 +973,20 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
       Mh[h] = h < p.g ? sM[h] : 0.f;
       iL[h] = h < p.g ? sInvL[h] : 0.f;
     }
+    auto score = [&](float4 x0, float4 x1) -> float {
+      const float xv[kSlots] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      float sg = 0.f;
+#pragma unroll
+      for (int h = 0; h < kSlots; ++h)
+        if (h < p.g) sg = fmaf(fast_exp2(xv[h] - Mh[h]), iL[h], sg);
+      return sg;
+    };
     const size_t unit = (size_t)b * p.Hkv + hkv;
     float* sp = p.sigma_part + unit * p.max_img;
-    const int nper = (c.n_img + S - 1) / S;
-    const int i_lo = (int)rank * nper, i_hi = min(c.n_img, i_lo + nper);
+    const int img_end = c.img_start + c.n_img;
+    // a focal text list is [0, N_t - 1): text index = position
+    const int i_lo = max(c.txt_lo, c.img_start) - c.img_start;
+    const int i_hi = min(c.txt_lo + c.n_txt, img_end) - c.img_start;
     for (int i0 = i_lo; i0 < i_hi; i0 += 4 * kThreads) {
       float4 x[4][2];
 #pragma unroll
@@ -976,14 +999,14 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int i = i0 + u * kThreads + tid;
-        const float xv[kSlots] = {x[u][0].x, x[u][0].y, x[u][0].z, x[u][0].w,
-                                  x[u][1].x, x[u][1].y, x[u][1].z, x[u][1].w};
-        float sg = 0.f;
-#pragma unroll
-        for (int h = 0; h < kSlots; ++h)
-          if (h < p.g) sg = fmaf(fast_exp2(xv[h] - Mh[h]), iL[h], sg);
+        const float sg = score(x[u][0], x[u][1]);
         if (i < i_hi) sp[i] = sg;
       }
+    }
+    if (c.has_cur && tid == 0 && c.cur_pos >= c.img_start && c.cur_pos < img_end) {
+      const int i = c.cur_pos - c.img_start;
+      const float4* src4 = reinterpret_cast<const float4*>(logit_base + (size_t)i * kSlots);
+      sp[i] = score(__ldcg(src4), __ldcg(src4 + 1));
     }
   }
 }

@@ -246,7 +246,9 @@ struct Smem {
   static constexpr int kRecvMl = kPosOffset + kSliceMax * 4;         // f32 [kMaxSplits][8][2]
   static constexpr int kRecvAcc = kRecvMl + kMaxSplits * kSlots * 2 * 4;
   static constexpr int kRecvAccFloats = 4 * (kSlots * D / 4 + kMaxSplits);
-  static constexpr int kQOffset = kRecvAcc + kRecvAccFloats * 4;     // f32 path: q[8][D]
+  // the CTA's one reading of k before the wait (sparse), shared by its threads
+  static constexpr int kSpecK = kRecvAcc + kRecvAccFloats * 4;
+  static constexpr int kQOffset = kSpecK + 16;                       // f32 path: q[8][D]
   static constexpr int kMainBytes = kQOffset + (sizeof(T) == 4 ? kSlots * D * 4 : 0);
 };
 
@@ -271,12 +273,14 @@ inline int attend_smem_bytes() {
 // Split-K factor S (= cluster size) for `units` (sequence, KV head) pairs and
 // attend lists of at most `len` tokens; active[s] = clusters of s CTAs the
 // device holds at once. Model: a CTA streams its share of len/S tokens at
-// ~13 ns per token (a 512-byte K+V row at ~40 GB/s per CTA), slowed down when
-// a wave of CTAs together asks for more than HBM delivers; clusters run in
-// waves of active[S]; every doubling of the cluster adds ~1 us of merge and
-// barrier latency.
+// ~8 ns per token when it runs alone, slowed down when a wave of CTAs
+// together asks for more than HBM delivers (~40 GB/s per CTA under load);
+// clusters run in waves of active[S]; every doubling of the cluster adds
+// ~1 us of merge and barrier latency. (Fitted to graph-replayed decode steps
+// on GB300: 1 sequence picks 4 splits for gather layers and 16 for full
+// ones, 32 sequences 2 and 2.)
 inline int choose_splits(long units, long len, int max_splits, const int* active) {
-  const double ns_per_token = 13.0, cta_gbs = 40.0, hbm_gbs = 6500.0, us_per_doubling = 1.0;
+  const double ns_per_token = 8.0, cta_gbs = 40.0, hbm_gbs = 6500.0, us_per_doubling = 1.0;
   if (len < 1) len = 1;
   int best = 1;
   double best_cost = 1e300;
