@@ -69,6 +69,7 @@ def _load() -> ctypes.CDLL:
         "fastocr_profiler_select": ([P, I32, ctypes.POINTER(I32), ctypes.POINTER(F64), P], I32),
         "fastocr_device_status": ([P, ctypes.POINTER(I32), P], I32),
         "fastocr_set_splits": ([P, I32, I32], I32),
+        "fastocr_set_length_hint": ([P, I32], I32),
         "fastocr_focal_attend_noalloc": ([ctypes.POINTER(fastocr_dims), P,
                                           ctypes.POINTER(fastocr_kv), P, F64, P, P, I32, P, P, P],
                                          I32),
@@ -175,6 +176,10 @@ def fastocr_device_status(handle, stream=None) -> int:
     _check("fastocr_device_status",
            lib.fastocr_device_status(handle, ctypes.byref(s), _stream(stream)))
     return int(s.value)
+
+
+def fastocr_set_length_hint(handle, n_t) -> None:
+    _check("fastocr_set_length_hint", lib.fastocr_set_length_hint(handle, int(n_t)))
 
 
 def fastocr_set_splits(handle, mode, splits) -> None:

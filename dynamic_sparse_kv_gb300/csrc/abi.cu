@@ -31,6 +31,7 @@ struct fastocr_handle {
   int split_override[3];
   int max_splits;   // largest thread-block cluster the device co-schedules (<= 16)
   int active[kMaxSplits + 1];   // clusters of each size the device holds at once
+  long len_hint;    // caller's N_t of the coming calls (0: unknown), split choice only
   void* ws;
   size_t ws_bytes;
   float* logits;
@@ -55,11 +56,16 @@ int splits_for(const fastocr_handle* h, int mode_slot, long len) {
   const int o = h->split_override[mode_slot];
   return o > 0 ? std::min(o, h->max_splits)
                : choose_splits((long)h->dims.batch * h->dims.num_kv_heads, len, h->max_splits,
-                               h->active);
+                               h->active, h->num_sms);
 }
 
 long max_tokens(const fastocr_handle* h) {
   return (long)h->dims.max_pages_per_seq << h->log2_page;
+}
+
+// cache length the split choice assumes: the caller's hint, else the capacity
+long expected_tokens(const fastocr_handle* h) {
+  return h->len_hint > 0 ? std::min(h->len_hint, max_tokens(h)) : max_tokens(h);
 }
 
 fastocr_status check_kv(const fastocr_handle* h, const fastocr_kv* kv) {
@@ -210,7 +216,7 @@ fastocr_status fastocr_full_attend(fastocr_handle* h, const void* q, const fasto
   if (st != FASTOCR_OK) return st;
   if (!aligned16(q) || !aligned16(out)) return FASTOCR_ERR_ALIGN;
   Params p = base_params(h, q, kv, out);
-  p.splits = splits_for(h, 0, max_tokens(h));
+  p.splits = splits_for(h, 0, expected_tokens(h));
   return launch(h, kFull, p, stream);
 }
 
@@ -233,7 +239,7 @@ fastocr_status fastocr_focal_attend(fastocr_handle* h, const void* q, const fast
   p.idx_stride = idx_stride;
   p.k_out = k_out;
   p.profile_layer = profile_layer;
-  p.splits = splits_for(h, 0, max_tokens(h));
+  p.splits = splits_for(h, 0, expected_tokens(h));
   return launch(h, kFocal, p, stream);
 }
 
@@ -252,8 +258,8 @@ fastocr_status fastocr_sparse_attend(fastocr_handle* h, const void* q, const fas
   p.idx_stride = idx_stride;
   p.k_in = k;
   // text tokens (cache minus the image) plus at most idx_stride selected ones
-  const long text = std::max(0L, max_tokens(h) - (long)h->dims.max_img_tokens);
-  p.splits = splits_for(h, 1, std::min(max_tokens(h), text + idx_stride));
+  const long text = std::max(0L, expected_tokens(h) - (long)h->dims.max_img_tokens);
+  p.splits = splits_for(h, 1, std::min(expected_tokens(h), text + idx_stride));
   return launch(h, kSparse, p, stream);
 }
 
@@ -268,7 +274,7 @@ fastocr_status fastocr_rswa_attend(fastocr_handle* h, const void* q, const fasto
   Params p = base_params(h, q, kv, out);
   p.prefix_len = prefix_len;
   p.window = window;
-  p.splits = splits_for(h, 2, std::min(max_tokens(h), (long)prefix_len + window));
+  p.splits = splits_for(h, 2, std::min(expected_tokens(h), (long)prefix_len + window));
   return launch(h, kRswa, p, stream);
 }
 
@@ -311,6 +317,13 @@ fastocr_status fastocr_device_status(fastocr_handle* h, int32_t* status, fastocr
       cudaMemsetAsync(h->status, 0, sizeof(int32_t), s) != cudaSuccess)
     return FASTOCR_ERR_CUDA;
   *status = v;
+  return FASTOCR_OK;
+}
+
+fastocr_status fastocr_set_length_hint(fastocr_handle* h, int32_t n_t) {
+  if (!h) return FASTOCR_ERR_NULL;
+  if (n_t < 0) return FASTOCR_ERR_INVALID;
+  h->len_hint = n_t;
   return FASTOCR_OK;
 }
 

@@ -845,6 +845,23 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
   if (bad) atomicOr(p.status, bad);
   __syncthreads();
 
+  // focal: this CTA's image tokens and the logits of its first 4*kThreads of
+  // them, loaded now so that the load latency hides behind the merge
+  const int img_end = c.img_start + c.n_img;
+  // a focal text list is [0, N_t - 1): text index = position
+  const int sg_lo = max(c.txt_lo, c.img_start) - c.img_start;
+  const int sg_hi = min(c.txt_lo + c.n_txt, img_end) - c.img_start;
+  float4 sgx[4][2];
+  if constexpr (MODE == kFocal) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = sg_lo + u * kThreads + tid;
+      const float4* src4 = reinterpret_cast<const float4*>(logit_base + (size_t)i * kSlots);
+      sgx[u][0] = i < sg_hi ? __ldcg(src4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      sgx[u][1] = i < sg_hi ? __ldcg(src4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+
   // ---------------- push the CTA partial to the CTAs of the cluster
   // CTA `r` of the S splits owns output pairs [r*per, (r+1)*per) of the
   // (head, 4 dims) pairs; every CTA writes its share of each owner's pairs,
@@ -983,24 +1000,21 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
     };
     const size_t unit = (size_t)b * p.Hkv + hkv;
     float* sp = p.sigma_part + unit * p.max_img;
-    const int img_end = c.img_start + c.n_img;
-    // a focal text list is [0, N_t - 1): text index = position
-    const int i_lo = max(c.txt_lo, c.img_start) - c.img_start;
-    const int i_hi = min(c.txt_lo + c.n_txt, img_end) - c.img_start;
-    for (int i0 = i_lo; i0 < i_hi; i0 += 4 * kThreads) {
-      float4 x[4][2];
+    for (int i0 = sg_lo; i0 < sg_hi; i0 += 4 * kThreads) {
+      if (i0 > sg_lo) {   // later blocks of 4*kThreads tokens
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * kThreads + tid;
-        const float4* src4 = reinterpret_cast<const float4*>(logit_base + (size_t)i * kSlots);
-        x[u][0] = i < i_hi ? __ldcg(src4) : make_float4(0.f, 0.f, 0.f, 0.f);
-        x[u][1] = i < i_hi ? __ldcg(src4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * kThreads + tid;
+          const float4* src4 = reinterpret_cast<const float4*>(logit_base + (size_t)i * kSlots);
+          sgx[u][0] = i < sg_hi ? __ldcg(src4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          sgx[u][1] = i < sg_hi ? __ldcg(src4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int i = i0 + u * kThreads + tid;
-        const float sg = score(x[u][0], x[u][1]);
-        if (i < i_hi) sp[i] = sg;
+        const float sg = score(sgx[u][0], sgx[u][1]);
+        if (i < sg_hi) sp[i] = sg;
       }
     }
     if (c.has_cur && tid == 0 && c.cur_pos >= c.img_start && c.cur_pos < img_end) {

@@ -271,16 +271,20 @@ inline int attend_smem_bytes() {
 }
 
 // Split-K factor S (= cluster size) for `units` (sequence, KV head) pairs and
-// attend lists of at most `len` tokens; active[s] = clusters of s CTAs the
-// device holds at once. Model: a CTA streams its share of len/S tokens at
-// ~8 ns per token when it runs alone, slowed down when a wave of CTAs
-// together asks for more than HBM delivers (~40 GB/s per CTA under load);
-// clusters run in waves of active[S]; every doubling of the cluster adds
-// ~1 us of merge and barrier latency. (Fitted to graph-replayed decode steps
-// on GB300: 1 sequence picks 4 splits for gather layers and 16 for full
-// ones, 32 sequences 2 and 2.)
-inline int choose_splits(long units, long len, int max_splits, const int* active) {
-  const double ns_per_token = 8.0, cta_gbs = 40.0, hbm_gbs = 6500.0, us_per_doubling = 1.0;
+// attend lists of about `len` tokens; active[s] = clusters of s CTAs the
+// device holds at once, num_sms its SM count. Model: a CTA streams its share
+// of len/S tokens at ~8 ns per token when it runs alone, slowed down when a
+// wave of CTAs together asks for more than HBM delivers (~40 GB/s per CTA
+// under load); clusters run in waves of active[S]; every doubling of the
+// cluster adds ~0.35 us of merge and barrier latency; a grid of at most
+// num_sms CTAs also lets the next kernel's CTAs stage their first tiles
+// while it runs (programmatic dependent launch), worth ~1.5 us. Fitted to
+// graph-replayed decode steps on GB300 (1 sequence: 4-6 splits for gather
+// layers, 16 for full ones; 32 sequences: 1 and 2; 8 sequences of 16k
+// image tokens: 4 for gather layers).
+inline int choose_splits(long units, long len, int max_splits, const int* active, int num_sms) {
+  const double ns_per_token = 8.0, cta_gbs = 40.0, hbm_gbs = 6500.0, us_per_doubling = 0.35,
+               overlap_us = 1.5;
   if (len < 1) len = 1;
   int best = 1;
   double best_cost = 1e300;
@@ -291,7 +295,8 @@ inline int choose_splits(long units, long len, int max_splits, const int* active
     const long ctas_in_wave = (units < act ? units : (long)act) * s;
     const double slow = ctas_in_wave * cta_gbs / hbm_gbs > 1.0 ? ctas_in_wave * cta_gbs / hbm_gbs : 1.0;
     const double per_cta_us = ((len + s - 1) / s) * ns_per_token * 1e-3 * slow;
-    const double cost = waves * per_cta_us + us_per_doubling * log2((double)s);
+    double cost = waves * per_cta_us + us_per_doubling * log2((double)s);
+    if (units * s <= num_sms) cost -= overlap_us;
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = s;

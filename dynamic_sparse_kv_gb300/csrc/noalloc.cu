@@ -149,10 +149,11 @@ extern "C" fastocr_status fastocr_focal_attend_noalloc(
   p.profile_layer = -1;
   p.status = status;
   p.max_img = d.max_img_tokens;
-  // same split rule as fastocr_focal_attend
+  // same split rule as fastocr_focal_attend on a handle without a length hint
   const int wide = d.head_dim == 128 ? 1 : 0;
   p.splits = choose_splits((long)d.batch * d.num_kv_heads, (long)d.max_pages_per_seq << log2_page,
-                           st->max_cluster[d.dtype][wide], st->active[d.dtype][wide]);
+                           st->max_cluster[d.dtype][wide], st->active[d.dtype][wide],
+                           st->num_sms);
   p.pdl_early = (long)p.splits * p.Hkv * p.B <= st->num_sms;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const cudaError_t e = d.dtype == FASTOCR_DTYPE_BF16 ? launch_bf16(d.head_dim, kFocal, p, cs)

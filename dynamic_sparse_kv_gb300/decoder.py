@@ -87,9 +87,11 @@ class DecodeAttention:
 
     # ------------------------------------------------------------ set-up
     def set_seq_len(self, n_t):
-        """N_t of the current step, int (all sequences) or [B] tensor."""
+        """N_t of the current step, int (all sequences) or [B] tensor. An int
+        also becomes the handle's length hint (split choice only)."""
         if isinstance(n_t, int):
             self.seq_len.fill_(n_t)
+            N.fastocr_set_length_hint(self.handle, n_t)
         else:
             self.seq_len.copy_(n_t, non_blocking=True)
 

@@ -190,6 +190,14 @@ fastocr_status fastocr_profiler_select(fastocr_handle* h, int32_t n_focal, int32
  * (host) and clear it. Synchronises `stream`. */
 fastocr_status fastocr_device_status(fastocr_handle* h, int32_t* status, fastocr_stream stream);
 
+/* Tell the handle the cache length N_t (tokens per sequence, the largest in
+ * the batch) that the coming calls will see; 0 clears the hint. Only the
+ * choice of the split-K factor uses it (without a hint it assumes a full
+ * cache of max_pages_per_seq*page_size tokens); results do not depend on it,
+ * and a wrong hint only costs speed. A call captured in a CUDA graph keeps
+ * the split factor chosen at capture. */
+fastocr_status fastocr_set_length_hint(fastocr_handle* h, int32_t n_t);
+
 /* Override the split-K factor of a mode (0 = full/focal, 1 = sparse,
  * 2 = R-SWA); 0 restores the automatic choice. Splits are clamped to
  * [1, 16] (the splits of one sequence and KV head form one thread-block

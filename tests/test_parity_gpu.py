@@ -278,3 +278,41 @@ def test_host_argument_errors():
     with pytest.raises(N.FastOCRError) as e:
         N.fastocr_rswa_attend(dec.handle, q, dec.kv[0], -1, 4, out)
     assert e.value.status == N.FASTOCR_ERR_INVALID
+    with pytest.raises(N.FastOCRError) as e:
+        N.fastocr_set_length_hint(dec.handle, -5)
+    assert e.value.status == N.FASTOCR_ERR_INVALID
+    with pytest.raises(N.FastOCRError) as e:
+        N.fastocr_set_splits(dec.handle, 3, 2)
+    assert e.value.status == N.FASTOCR_ERR_INVALID
+
+
+def test_length_hint_changes_speed_not_results():
+    """Any length hint (none, exact, far too small, far too large) gives the same
+    outputs and selection up to summation order; forced split counts likewise."""
+    from dynamic_sparse_kv_gb300 import _native as N
+    case = _case("qwen7b_b1", batch=3, layers=1, prompt=40, grid=(1, 24, 24), steps=12, tau=0.05)
+    wl = case.wl
+    n_t = wl.seq_len_at(11)
+    q = case.q_at(11)[0].contiguous()
+    dec = _direct(case, n_t)
+    kv = KVCache(case)
+    for hint in (0, n_t, 1, 1 << 20):
+        N.fastocr_set_length_hint(dec.handle, hint)
+        out_f, out_s = torch.empty_like(q), torch.empty_like(q)
+        idx = torch.zeros(wl.batch, dec.stride, dtype=torch.int32, device="cuda")
+        k = torch.zeros(wl.batch, dtype=torch.int32, device="cuda")
+        N.fastocr_focal_attend(dec.handle, q, dec.kv[0], case.img_range, wl.tau, out_f, idx,
+                               dec.stride, k)
+        N.fastocr_sparse_attend(dec.handle, q, dec.kv[0], case.img_range, idx, dec.stride, k,
+                                out_s)
+        torch.cuda.synchronize()
+        for b in range(wl.batch):
+            Kl, Vl = kv(0, b)
+            qb = np64(q[b])
+            ref_out, ref_sel, sigma = A.focal_attend(qb, Kl, Vl, n_t, wl.prompt, wl.n_img, wl.tau)
+            assert_close(out_f[b], ref_out, TOL["bf16"], f"focal hint={hint} b={b}")
+            got = idx[b, :int(k[b])].cpu().numpy()
+            check_selection(got, ref_sel, sigma, wl.prompt, f"hint={hint} b={b}")
+            assert_close(out_s[b], A.sparse_attend(qb, Kl, Vl, n_t, wl.prompt, wl.n_img, got),
+                         TOL["bf16"], f"sparse hint={hint} b={b}")
+    assert dec.device_status() == 0

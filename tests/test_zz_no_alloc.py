@@ -47,6 +47,7 @@ def test_noalloc_matches_handle_path(name, overrides):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     for t in (2, 5):                       # two calls in a row
         dec.set_seq_len(wl.seq_len_at(t))
+        N.fastocr_set_length_hint(dec.handle, 0)   # same split rule as the no-alloc call
         q = case.q_at(t)[layer].contiguous()
         out_ref, out = torch.empty_like(q), torch.full_like(q, float("nan"))
         idx_ref = torch.zeros(wl.batch, dec.stride, dtype=torch.int32, device="cuda")
