@@ -10,5 +10,6 @@ from . import _native  # noqa: F401  (loads libfastocr.so or raises)
 from ._native import (  # noqa: F401
     fastocr_abi_version, fastocr_create, fastocr_destroy, fastocr_device_status,
     fastocr_focal_attend, fastocr_full_attend, fastocr_profiler_reset, fastocr_profiler_select,
-    fastocr_rswa_attend, fastocr_set_splits, fastocr_sparse_attend, make_kv)
-from .decoder import CapturedStep, DecodeAttention, keep_capacity  # noqa: F401
+    fastocr_rswa_attend, fastocr_set_length_hint, fastocr_set_splits, fastocr_sparse_attend,
+    make_kv)
+from .decoder import CapturedStep, DecodeAttention, keep_capacity, ring_block_table  # noqa: F401

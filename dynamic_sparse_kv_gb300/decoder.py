@@ -34,6 +34,34 @@ def keep_capacity(tau: float, n_img: int) -> int:
     return max(1, min(n_img, int(math.ceil(tau * n_img)) + 1)) if n_img > 0 else 1
 
 
+def ring_block_table(batch: int, prefix_len: int, window: int, page_size: int, max_tokens: int,
+                     first_page: int = 0):
+    """Block table that keeps an R-SWA cache in bounded memory (Unlimited OCR
+    page, "R-SWA": the attend set is the global prefix plus a sliding window,
+    so only those tokens need storage).
+
+    Logical page j of sequence b maps to physical page
+    first_page + b*P + (j if j < P0 else P0 + (j - P0) % R), with P0 =
+    ceil(prefix_len / page_size) prefix pages, R = max(1, ceil(window /
+    page_size)) ring pages and P = P0 + R pages per sequence, whatever
+    max_tokens is. The caller writes token p's K/V to
+    (table[b, p // page_size], p % page_size) as usual. Token p shares its
+    row only with tokens p +- m*R*page_size, and R*page_size >= window, so a
+    row is overwritten only after its token has left the window
+    [N_t - window, N_t); the R-SWA kernels read nothing else outside the
+    prefix. Returns (table [batch, ceil(max_tokens / page_size)] int32 on the
+    CPU, P).
+    """
+    p0 = -(-prefix_len // page_size)
+    ring = max(1, -(-window // page_size))
+    per = p0 + ring
+    n_pages = -(-max_tokens // page_size)
+    j = torch.arange(n_pages, dtype=torch.int64)
+    local = torch.where(j < p0, j, p0 + (j - p0) % ring)
+    table = first_page + torch.arange(batch, dtype=torch.int64)[:, None] * per + local[None, :]
+    return table.to(torch.int32), per
+
+
 class DecodeAttention:
     """Decode attention of a stack of layers over a paged KV cache.
 
