@@ -16,6 +16,8 @@ cudaError_t launch_f32(int head_dim, int mode, const Params& p, cudaStream_t s);
 cudaError_t prepare_bf16();
 cudaError_t prepare_f32();
 int max_cluster_bf16(int head_dim);
+int max_cluster_deep_bf16(int head_dim);
+int max_cluster_deep_f32(int head_dim);
 int max_cluster_f32(int head_dim);
 int active_clusters_bf16(int head_dim, int cluster);
 int active_clusters_f32(int head_dim, int cluster);
@@ -30,6 +32,7 @@ struct fastocr_handle {
   int log2_page;
   int split_override[3];
   int max_splits;   // largest thread-block cluster the device co-schedules (<= 16)
+  int max_splits_deep;   // same for the one-CTA-per-SM variant (0: none)
   int active[kMaxSplits + 1];   // clusters of each size the device holds at once
   long len_hint;    // caller's N_t of the coming calls (0: unknown), split choice only
   void* ws;
@@ -111,6 +114,9 @@ fastocr_status launch(const fastocr_handle* h, int mode, Params p, fastocr_strea
   // while this one runs); grids that need the whole GPU release it only
   // after their main loop, so its CTAs do not take slots from this grid
   p.pdl_early = (long)p.splits * p.Hkv * p.B <= h->num_sms;
+  // grids that leave room for the next kernel's CTAs at one CTA per SM take
+  // the deeper pipeline (more of each CTA's tiles staged before the wait)
+  p.deep = 2L * p.splits * p.Hkv * p.B <= h->num_sms && p.splits <= h->max_splits_deep;
   cudaError_t e = h->dims.dtype == FASTOCR_DTYPE_BF16 ? launch_bf16(h->dims.head_dim, mode, p, s)
                                                        : launch_f32(h->dims.head_dim, mode, p, s);
   return e == cudaSuccess ? FASTOCR_OK : FASTOCR_ERR_CUDA;
@@ -178,6 +184,8 @@ fastocr_status fastocr_create(const fastocr_dims* dims, fastocr_handle** out) {
   h->log2_page = log2_page;
   h->max_splits = d.dtype == FASTOCR_DTYPE_BF16 ? max_cluster_bf16(d.head_dim)
                                                 : max_cluster_f32(d.head_dim);
+  h->max_splits_deep = d.dtype == FASTOCR_DTYPE_BF16 ? max_cluster_deep_bf16(d.head_dim)
+                                                     : max_cluster_deep_f32(d.head_dim);
   for (int c = 1; c <= h->max_splits; ++c)
     h->active[c] = d.dtype == FASTOCR_DTYPE_BF16 ? active_clusters_bf16(d.head_dim, c)
                                                  : active_clusters_f32(d.head_dim, c);

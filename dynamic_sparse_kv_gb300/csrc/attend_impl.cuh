@@ -82,7 +82,9 @@ __global__ void __launch_bounds__(NT) select_kernel(const Params p) {
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + u * NT + tid;
       const bool act = i < n;
-      const uint32_t key = __float_as_uint(sv[u]);
+      // scores are >= 0, so the bit pattern without its (zero) sign bit keeps
+      // their order; the first 8-bit digit is then the whole exponent
+      const uint32_t key = __float_as_uint(sv[u]) << 1;
       if (act) {
         keys[i] = key;
         if (profiling) local += (double)sv[u];
@@ -338,10 +340,12 @@ __device__ __forceinline__ void add_selection(const Params& p, int k, int split,
   c.n_sel = max(0, min(per, k - c.sel_lo));
 }
 
-template <typename T, int D, int MODE>
+// ST: cp.async pipeline depth per warp (kStages, or kStagesDeep for grids
+// small enough that every CTA has an SM of its own).
+template <typename T, int D, int MODE, int ST>
 __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  using SM = Smem<T, D>;
+  using SM = Smem<T, D, ST>;
   using E = EpiSmem<D>;
   constexpr bool kMma = sizeof(T) == 2;
   constexpr int ROWB = SM::kRowBytes;
@@ -355,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
   const T* __restrict__ vg = static_cast<const T*>(p.v);
   const int32_t* __restrict__ bt = p.block_table + (size_t)b * p.max_pages;
   const int page_mask = (1 << p.log2_page) - 1;
-  unsigned char* pipe = smem + warp * kStages * SM::kStageBytes;
+  unsigned char* pipe = smem + warp * ST * SM::kStageBytes;
   int* srow = reinterpret_cast<int*>(smem + SM::kRowOffset);
   int* spos = reinterpret_cast<int*>(smem + SM::kPosOffset);
 
@@ -429,14 +433,25 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
   static_assert(CH <= 32 && 32 % CH == 0, "a row must fit one warp instruction");
   const int n_rows = (p.num_pages * p.Hkv) << p.log2_page;   // < 2^31, checked on the host
   constexpr int kRowsPerInst = 32 / CH;
+  constexpr int kIss = kTile / kRowsPerInst;   // instructions per 16 rows
   const int ch_lane = lane % CH, row_lane = lane / CH;
+  // lane constants of the copies: this lane's chunk of K and V rows, and its
+  // swizzled destination offset in each of its kIss rows of a stage
+  const char* kg_lane = reinterpret_cast<const char*>(kg) + ch_lane * 16;
+  const char* vg_lane = reinterpret_cast<const char*>(vg) + ch_lane * 16;
+  uint32_t doff[kIss];
+#pragma unroll
+  for (int i = 0; i < kIss; ++i) {
+    const int r = i * kRowsPerInst + row_lane;
+    doff[i] = r * ROWB + ((ch_lane ^ (r & 7)) << 4);
+  }
   auto issue = [&](int j, int n_round) {
-    const int stage = j % kStages;
+    const int stage = j % ST;
     const int base = (warp + j * kWarps) * kTile;
     const uint32_t sb = smem_u32(pipe + stage * SM::kStageBytes);
-    int rows[kTile / kRowsPerInst];
+    int rows[kIss];
 #pragma unroll
-    for (int i = 0; i < kTile / kRowsPerInst; ++i) {
+    for (int i = 0; i < kIss; ++i) {
       const int r = i * kRowsPerInst + row_lane;
       rows[i] = base + r < n_round ? srow[base + r] : -1;
       if (rows[i] >= n_rows) {   // never true for a resolved row; guards the copy anyway
@@ -445,13 +460,11 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
       }
     }
 #pragma unroll
-    for (int i = 0; i < kTile / kRowsPerInst; ++i) {
-      const int r = i * kRowsPerInst + row_lane;
-      const size_t off = (size_t)max(rows[i], 0) * D + ch_lane * kElemPerChunk;
+    for (int i = 0; i < kIss; ++i) {
+      const size_t off = (size_t)max(rows[i], 0) * ROWB;
       const int bytes = rows[i] >= 0 ? 16 : 0;
-      const uint32_t dst = sb + r * ROWB + ((ch_lane ^ (r & 7)) << 4);
-      cp_async16(dst, kg + off, bytes);
-      cp_async16(dst + kTile * ROWB, vg + off, bytes);
+      cp_async16(sb + doff[i], kg_lane + off, bytes);
+      cp_async16(sb + doff[i] + kTile * ROWB, vg_lane + off, bytes);
     }
   };
 
@@ -480,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
     n_sel_pad = (c.n_sel + kTile - 1) / kTile * kTile;
     spec_u1 = min(kSliceMax, n_txt_pad + c.n_sel);
     const int u_pad = min(kSliceMax, n_txt_pad + n_sel_pad);
-    const int u_staged = kWarps * kStages * kTile;   // entries the pre-wait tiles can cover
+    const int u_staged = kWarps * ST * kTile;   // entries the pre-wait tiles can cover
     int pos[kPer], page[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
@@ -524,8 +537,8 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
   }
   __syncthreads();
   int pre_issued = 0;   // leading tiles of this warp already staged
-#pragma unroll
-  for (int j = 0; j < kStages; ++j) {
+#pragma unroll 1
+  for (int j = 0; j < ST; ++j) {
     const int end = (warp + j * kWarps + 1) * kTile;
     if (pre_issued == j && end <= n_pre) {
       issue(j, n_pre);
@@ -543,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
   // the speculation fails).
   if (c.has_cur && n_pre < kSliceMax) {
     const int t_cur = n_pre / kTile;   // n_pre is a multiple of kTile here
-    if (warp == t_cur % kWarps && pre_issued == t_cur / kWarps && pre_issued < kStages) {
+    if (warp == t_cur % kWarps && pre_issued == t_cur / kWarps && pre_issued < ST) {
       issue(pre_issued, n_pre + 1);
       cp_async_commit();
       ++pre_issued;
@@ -624,6 +637,19 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
   }
   __syncthreads();
 
+  // lane constants of the ldmatrix addresses within a stage (bf16): K reads
+  // row `lane & 15`, chunk 2ks + (lane >> 4); V reads row
+  // (lane & 7) + 8 (lane >> 4), chunk 2mt + ((lane >> 3) & 1). Chunk bit 3
+  // (ks, mt >= 4) is untouched by the swizzle: 128 bytes added per 4 steps.
+  uint32_t koff[4], voff[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int kr = (lane & 7) + (lane & 8), kc = 2 * q + (lane >> 4);
+    koff[q] = kr * ROWB + ((kc ^ (kr & 7)) << 4);
+    const int vr = (lane & 7) + ((lane >> 4) << 3), vc = 2 * q + ((lane >> 3) & 1);
+    voff[q] = vr * ROWB + ((vc ^ (vr & 7)) << 4);
+  }
+
   // ---------------- stream the work list in rounds of kSliceMax entries
   for (int rb = 0; rb < n_cta; rb += kSliceMax) {
     const int n_round = min(n_cta - rb, kSliceMax);
@@ -636,19 +662,19 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
     }
     const int n_tiles = (n_round + kTile - 1) / kTile;
     const int my_tiles = n_tiles > warp ? (n_tiles - warp + kWarps - 1) / kWarps : 0;
-#pragma unroll
-    for (int j = 0; j < kStages - 1; ++j) {
+#pragma unroll 1
+    for (int j = 0; j < ST - 1; ++j) {
       if (j < first) continue;
       if (j < my_tiles) issue(j, n_round);
       cp_async_commit();
     }
     for (int it = 0; it < my_tiles; ++it) {
-      const int jn = it + kStages - 1;   // tiles below `first` were staged already
+      const int jn = it + ST - 1;   // tiles below `first` were staged already
       if (jn >= first && jn < my_tiles) issue(jn, n_round);
       cp_async_commit();
-      cp_async_wait<kStages - 1>();
+      cp_async_wait<ST - 1>();
       __syncwarp();
-      const int stage = it % kStages;
+      const int stage = it % ST;
       unsigned char* kS = pipe + stage * SM::kStageBytes;
       unsigned char* vS = kS + kTile * ROWB;
       const int tbase = (warp + it * kWarps) * kTile;   // tile start within the round
@@ -664,10 +690,10 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
         const uint32_t kA = smem_u32(kS), vA = smem_u32(vS);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const int row = (lane & 7) + (lane & 8);
-          const int ch = 2 * ks + (lane >> 4);
+          // chunk 2ks + (lane >> 4) of row `lane & 15`, swizzled: a lane
+          // constant for ks % 4 plus 8 chunks per 4 ks
           uint32_t a[4];
-          ldmatrix_x4(a, kA + row * ROWB + ((ch ^ (row & 7)) << 4));
+          ldmatrix_x4(a, kA + koff[ks & 3] + (ks >> 2) * 128);
           mma_bf16(cc[ks % kChains], a, sm_.qf[ks][0], sm_.qf[ks][1]);
         }
         float cfr[4];
@@ -727,10 +753,8 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
         const uint32_t bb1 = movmatrix_trans(pack_bf16(p2, p3));
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
-          const int row = (lane & 7) + ((lane >> 4) << 3);
-          const int ch = 2 * mt + ((lane >> 3) & 1);
           uint32_t a[4];
-          ldmatrix_x4_trans(a, vA + row * ROWB + ((ch ^ (row & 7)) << 4));
+          ldmatrix_x4_trans(a, vA + voff[mt & 3] + (mt >> 2) * 128);
           // O^T[16 dims x 8 heads] += V^T[16 dims x 16 keys] . P^T[16 keys x 8 heads]
           mma_bf16(sm_.acc[mt], a, bb0, bb1);
         }
@@ -1029,17 +1053,17 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
 // the previous kernel on the stream finishes its epilogue; it waits for that
 // kernel's completion (griddepcontrol.wait) before reading any global memory.
 // A focal layer is two launches: the attend kernel, then the selection kernel.
-template <typename T, int D, int MODE>
+template <typename T, int D, int MODE, int ST>
 cudaError_t launch_attend(const Params& p, cudaStream_t stream) {
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pdl_config(dim3(p.splits, p.Hkv, p.B), dim3(kThreads, 1, 1),
-                                      attend_smem_bytes<T, D>(), stream, attr);
+                                      attend_smem_bytes<T, D, ST>(), stream, attr);
   attr[1].id = cudaLaunchAttributeClusterDimension;   // the splits of one (b, hkv)
   attr[1].val.clusterDim.x = p.splits;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attend_kernel<T, D, MODE>, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attend_kernel<T, D, MODE, ST>, p);
   if (e != cudaSuccess || MODE != kFocal) return e;
   cudaLaunchAttribute attr2[1];
   cudaLaunchConfig_t cfg2 = pdl_config(dim3(p.B, 1, 1), dim3(kSelectThreads, 1, 1),
@@ -1049,24 +1073,42 @@ cudaError_t launch_attend(const Params& p, cudaStream_t stream) {
 
 // Raise the dynamic shared-memory limits once per device, before any launch
 // (so never inside a stream capture).
+// Every kernel of the library asks for the largest shared-memory carveout, so
+// that an SM never has to drain to change its shared-memory/L1 split between
+// two of them (the kernels keep no data in L1).
 template <typename Kern>
 cudaError_t prepare_attend(Kern k, int bytes) {
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
+
+template <typename T, int D, int ST>
+cudaError_t prepare_modes() {
+  const int bytes = attend_smem_bytes<T, D, ST>();
+  cudaError_t e;
+  if ((e = prepare_attend(attend_kernel<T, D, kFull, ST>, bytes))) return e;
+  if ((e = prepare_attend(attend_kernel<T, D, kFocal, ST>, bytes))) return e;
+  if ((e = prepare_attend(attend_kernel<T, D, kSparse, ST>, bytes))) return e;
+  return prepare_attend(attend_kernel<T, D, kRswa, ST>, bytes);
 }
 
 template <typename T, int D>
 cudaError_t prepare_all_modes() {
-  const int bytes = attend_smem_bytes<T, D>();
   cudaError_t e;
-  if ((e = prepare_attend(attend_kernel<T, D, kFull>, bytes))) return e;
-  if ((e = prepare_attend(attend_kernel<T, D, kFocal>, bytes))) return e;
-  if ((e = prepare_attend(attend_kernel<T, D, kSparse>, bytes))) return e;
-  if ((e = prepare_attend(attend_kernel<T, D, kRswa>, bytes))) return e;
+  if ((e = prepare_modes<T, D, kStages>())) return e;
+  if constexpr (deep_fits<T, D>())
+    if ((e = prepare_modes<T, D, kStagesDeep>())) return e;
+  if ((e = cudaFuncSetAttribute(select_kernel<kSelectThreads>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                select_smem_bytes(kMaxImg))))
+    return e;
   return cudaFuncSetAttribute(select_kernel<kSelectThreads>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              select_smem_bytes(kMaxImg));
+                              cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
 }
 
 // How many clusters of `c` CTAs of this kernel the device holds at once (0 if
@@ -1085,21 +1127,23 @@ int active_clusters(int c) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, attend_kernel<T, D, kFull>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, attend_kernel<T, D, kFull, kStages>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   return n;
 }
 
-// Largest cluster (<= kMaxSplits) of this kernel that the device can co-schedule.
-template <typename T, int D>
+// Largest cluster (<= kMaxSplits) of this kernel that the device can
+// co-schedule (0: the variant does not exist).
+template <typename T, int D, int ST = kStages>
 int max_cluster_size() {
+  if constexpr (ST == kStagesDeep && !deep_fits<T, D>()) return 0;
   for (int c = kMaxSplits; c > 1; c >>= 1) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(c, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = attend_smem_bytes<T, D>();
+    cfg.dynamicSmemBytes = attend_smem_bytes<T, D, ST>();
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = c;
@@ -1108,22 +1152,29 @@ int max_cluster_size() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attend_kernel<T, D, kFull>, &cfg) == cudaSuccess && n > 0)
+    if (cudaOccupancyMaxActiveClusters(&n, attend_kernel<T, D, kFull, ST>, &cfg) == cudaSuccess && n > 0)
       return c;
     cudaGetLastError();
   }
   return 1;
 }
 
-template <typename T, int D>
-cudaError_t dispatch_mode(int mode, const Params& p, cudaStream_t s) {
+template <typename T, int D, int ST>
+cudaError_t dispatch_stages(int mode, const Params& p, cudaStream_t s) {
   switch (mode) {
-    case kFull: return launch_attend<T, D, kFull>(p, s);
-    case kFocal: return launch_attend<T, D, kFocal>(p, s);
-    case kSparse: return launch_attend<T, D, kSparse>(p, s);
-    case kRswa: return launch_attend<T, D, kRswa>(p, s);
+    case kFull: return launch_attend<T, D, kFull, ST>(p, s);
+    case kFocal: return launch_attend<T, D, kFocal, ST>(p, s);
+    case kSparse: return launch_attend<T, D, kSparse, ST>(p, s);
+    case kRswa: return launch_attend<T, D, kRswa, ST>(p, s);
   }
   return cudaErrorInvalidValue;
+}
+
+template <typename T, int D>
+cudaError_t dispatch_mode(int mode, const Params& p, cudaStream_t s) {
+  if constexpr (deep_fits<T, D>())
+    if (p.deep) return dispatch_stages<T, D, kStagesDeep>(mode, p, s);
+  return dispatch_stages<T, D, kStages>(mode, p, s);
 }
 
 }  // namespace fastocr

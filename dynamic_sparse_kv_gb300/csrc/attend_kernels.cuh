@@ -35,7 +35,8 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 16;      // tokens per warp tile
 constexpr int kSlots = 8;      // query-head slots per KV head (g <= 8)
-constexpr int kStages = 3;     // cp.async pipeline depth per warp
+constexpr int kStages = 3;     // cp.async pipeline depth per warp (two CTAs per SM)
+constexpr int kStagesDeep = 6; // depth of the variant for grids that leave an SM per CTA
 constexpr float kLazyMax = 8.f; // running-max slack (log2 units) before a rescale
 constexpr int kMaxSplits = 16;  // = the largest thread-block cluster used
 constexpr int kMaxImg = 16384; // image tokens whose scores fit in shared memory
@@ -75,6 +76,7 @@ struct Params {
   double* profile;           // [num_layers]
   int profile_layer;
   int pdl_early;             // grid fits on the SMs next to the next one: trigger it at once
+  int deep;                  // host: launch the kStagesDeep variant (one CTA per SM)
   int32_t* status;
   int max_img;
 };
@@ -234,11 +236,11 @@ __device__ __forceinline__ AttendList make_list(const Params& p, int b, int& bad
 
 constexpr int kSliceMax = 1024;  // work-list entries resolved to cache rows per round
 
-template <typename T, int D>
+template <typename T, int D, int ST = kStages>
 struct Smem {
   static constexpr int kRowBytes = D * (int)sizeof(T);
   static constexpr int kStageBytes = 2 * kTile * kRowBytes;          // K rows then V rows
-  static constexpr int kPipeBytes = kWarps * kStages * kStageBytes;
+  static constexpr int kPipeBytes = kWarps * ST * kStageBytes;
   static constexpr int kRowOffset = kPipeBytes;                      // int row[kSliceMax]
   static constexpr int kPosOffset = kRowOffset + kSliceMax * 4;      // int pos[kSliceMax]
   // partials pushed here by the other CTAs of the cluster (never overlaps
@@ -264,10 +266,16 @@ struct EpiSmem {
   static constexpr int kBytes = kInvL + kSlots * 4;
 };
 
-template <typename T, int D>
+template <typename T, int D, int ST = kStages>
 inline int attend_smem_bytes() {
-  static_assert(EpiSmem<D>::kBytes <= Smem<T, D>::kPipeBytes, "epilogue must fit the pipeline area");
-  return Smem<T, D>::kMainBytes;
+  static_assert(EpiSmem<D>::kBytes <= Smem<T, D, ST>::kPipeBytes, "epilogue must fit the pipeline area");
+  return Smem<T, D, ST>::kMainBytes;
+}
+
+// The deep variant exists where its shared memory fits one CTA.
+template <typename T, int D>
+constexpr bool deep_fits() {
+  return Smem<T, D, kStagesDeep>::kMainBytes <= 227 * 1024;
 }
 
 // Split-K factor S (= cluster size) for `units` (sequence, KV head) pairs and

@@ -20,6 +20,11 @@ int max_cluster_bf16(int head_dim) {
   return head_dim == 64 ? max_cluster_size<__nv_bfloat16, 64>() : max_cluster_size<__nv_bfloat16, 128>();
 }
 
+int max_cluster_deep_bf16(int head_dim) {
+  return head_dim == 64 ? max_cluster_size<__nv_bfloat16, 64, kStagesDeep>()
+                        : max_cluster_size<__nv_bfloat16, 128, kStagesDeep>();
+}
+
 int active_clusters_bf16(int head_dim, int cluster) {
   return head_dim == 64 ? active_clusters<__nv_bfloat16, 64>(cluster) : active_clusters<__nv_bfloat16, 128>(cluster);
 }

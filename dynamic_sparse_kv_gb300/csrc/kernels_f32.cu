@@ -20,6 +20,11 @@ int max_cluster_f32(int head_dim) {
   return head_dim == 64 ? max_cluster_size<float, 64>() : max_cluster_size<float, 128>();
 }
 
+int max_cluster_deep_f32(int head_dim) {
+  return head_dim == 64 ? max_cluster_size<float, 64, kStagesDeep>()
+                        : max_cluster_size<float, 128, kStagesDeep>();
+}
+
 int active_clusters_f32(int head_dim, int cluster) {
   return head_dim == 64 ? active_clusters<float, 64>(cluster) : active_clusters<float, 128>(cluster);
 }

@@ -25,6 +25,8 @@ int max_cluster_bf16(int head_dim);
 int max_cluster_f32(int head_dim);
 int active_clusters_bf16(int head_dim, int cluster);
 int active_clusters_f32(int head_dim, int cluster);
+int max_cluster_deep_bf16(int head_dim);
+int max_cluster_deep_f32(int head_dim);
 }  // namespace fastocr
 
 using namespace fastocr;
@@ -45,6 +47,7 @@ struct DeviceState {
   float* scratch;      // device address of g_scratch on this device
   int num_sms;
   int max_cluster[2][2];  // [dtype][head_dim == 128]
+  int max_cluster_deep[2][2];
   int active[2][2][kMaxSplits + 1];  // clusters of each size held at once
 };
 DeviceState g_state[kMaxDevices];
@@ -67,6 +70,10 @@ fastocr_status device_setup(int dev, DeviceState** out) {
     s.max_cluster[FASTOCR_DTYPE_F32][1] = max_cluster_f32(128);
     s.max_cluster[FASTOCR_DTYPE_BF16][0] = max_cluster_bf16(64);
     s.max_cluster[FASTOCR_DTYPE_BF16][1] = max_cluster_bf16(128);
+    s.max_cluster_deep[FASTOCR_DTYPE_F32][0] = max_cluster_deep_f32(64);
+    s.max_cluster_deep[FASTOCR_DTYPE_F32][1] = max_cluster_deep_f32(128);
+    s.max_cluster_deep[FASTOCR_DTYPE_BF16][0] = max_cluster_deep_bf16(64);
+    s.max_cluster_deep[FASTOCR_DTYPE_BF16][1] = max_cluster_deep_bf16(128);
     for (int dt = 0; dt < 2; ++dt)
       for (int wide = 0; wide < 2; ++wide)
         for (int c = 1; c <= s.max_cluster[dt][wide]; ++c)
@@ -155,6 +162,7 @@ extern "C" fastocr_status fastocr_focal_attend_noalloc(
                            st->max_cluster[d.dtype][wide], st->active[d.dtype][wide],
                            st->num_sms);
   p.pdl_early = (long)p.splits * p.Hkv * p.B <= st->num_sms;
+  p.deep = 2L * p.splits * p.Hkv * p.B <= st->num_sms && p.splits <= st->max_cluster_deep[d.dtype][wide];
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const cudaError_t e = d.dtype == FASTOCR_DTYPE_BF16 ? launch_bf16(d.head_dim, kFocal, p, cs)
                                                       : launch_f32(d.head_dim, kFocal, p, cs);
