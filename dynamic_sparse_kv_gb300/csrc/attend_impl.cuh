@@ -164,69 +164,70 @@ __global__ void __launch_bounds__(NT) select_kernel(const Params p) {
   // keep: (key & mask) > prefix, or == prefix for the first krem such keys
   const uint32_t thr = prefix;
 
-  // --- stable compaction: warp w owns offsets [w*per, (w+1)*per), read 32 at a time
-  const int per = ((n + NW - 1) / NW + 31) / 32 * 32;
-  const int lo = warp * per, hi = min(n, lo + per);
-  const uint32_t lt_mask = (1u << lane) - 1u;
+  // --- stable compaction: thread t owns the keys [t*per, t*per + per), per a
+  // multiple of 4 read as 16-byte vectors. An exclusive block scan of the
+  // packed (greater, equal) counts gives each thread its output offset: the
+  // kept keys before it are every greater key before it plus the first krem
+  // equal keys of the whole row.
+  const int per = ((n + NT - 1) / NT + 3) & ~3;
+  const int lo = tid * per, hi = min(n, lo + per);
   int gt = 0, eq = 0;
-  for (int base = lo; base < hi; base += 32) {
-    const int i = base + lane;
-    const bool ok = i < hi;
-    const uint32_t key = ok ? (keys[i] & mask) : 0u;
-    gt += __popc(__ballot_sync(0xffffffffu, ok && key > thr));
-    eq += __popc(__ballot_sync(0xffffffffu, ok && key == thr));
+  for (int i0 = lo; i0 < hi; i0 += 4) {
+    const uint4 kv = *reinterpret_cast<const uint4*>(keys + i0);
+    const uint32_t kk[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool ok = i0 + u < hi;
+      const uint32_t key = kk[u] & mask;
+      gt += ok && key > thr;
+      eq += ok && key == thr;
+    }
   }
-  int* s_gt = scratch + 8;
-  int* s_eq = scratch + 8 + NW;
-  if (lane == 0) {
-    s_gt[warp] = gt;
-    s_eq[warp] = eq;
+  int* s_warp = scratch + 8;           // [NW]: packed warp totals, then their exclusive prefix
+  const int packed = (gt << 16) | eq;  // both counts <= kMaxImg < 2^15
+  int incl = packed;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int t = lane < NW ? s_warp[lane] : 0;
+    int v = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane < NW) s_warp[lane] = v - t;
   }
   __syncthreads();
-  // exclusive scans over the warps, done by every warp with shuffles
-  int eq_before, out_before;
-  {
-    const int g_w = lane < NW ? s_gt[lane] : 0;
-    const int e_w = lane < NW ? s_eq[lane] : 0;
-    int e_incl = e_w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, e_incl, o);
-      if (lane >= o) e_incl += y;
-    }
-    const int e_excl = e_incl - e_w;
-    int take = krem - e_excl;
-    take = take < 0 ? 0 : (take > e_w ? e_w : take);
-    int o_incl = g_w + take;
-    const int mine = o_incl;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, o_incl, o);
-      if (lane >= o) o_incl += y;
-    }
-    eq_before = __shfl_sync(0xffffffffu, e_excl, warp);
-    out_before = __shfl_sync(0xffffffffu, o_incl - mine, warp);
-  }
+  const int before = s_warp[warp] + incl - packed;
+  int eq_run = before & 0xffff;
+  int out = (before >> 16) + min(eq_run, krem);
   int32_t* dst = p.idx_out + (size_t)b * p.idx_stride;
-  int eq_run = eq_before, out_run = out_before;
-  for (int base = lo; base < hi; base += 32) {
-    const int i = base + lane;
-    const bool ok = i < hi;
-    const uint32_t key = ok ? (keys[i] & mask) : 0u;
-    const bool is_gt = ok && key > thr, is_eq = ok && key == thr;
-    const uint32_t eq_b = __ballot_sync(0xffffffffu, is_eq);
-    const int my_eq_rank = eq_run + __popc(eq_b & lt_mask);
-    const bool take = is_gt || (is_eq && my_eq_rank < krem);
-    const uint32_t take_b = __ballot_sync(0xffffffffu, take);
-    const int slot = out_run + __popc(take_b & lt_mask);
-    if (take) {
-      if (slot < k)   // never false for a consistent selection; guards the store anyway
-        dst[slot] = L.img_start + i;
-      else
-        bad |= kDevInternal;
+  for (int i0 = lo; i0 < hi; i0 += 4) {
+    const uint4 kv = *reinterpret_cast<const uint4*>(keys + i0);
+    const uint32_t kk[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (i0 + u >= hi) break;
+      const uint32_t key = kk[u] & mask;
+      bool take = key > thr;
+      if (key == thr) {
+        take = eq_run < krem;
+        ++eq_run;
+      }
+      if (take) {
+        if (out < k)   // never false for a consistent selection; guards the store anyway
+          dst[out] = L.img_start + i0 + u;
+        else
+          bad |= kDevInternal;
+        ++out;
+      }
     }
-    eq_run += __popc(eq_b);
-    out_run += __popc(take_b);
   }
   if (bad & kDevInternal) atomicOr(p.status, kDevInternal);
 }
@@ -363,8 +364,9 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
   int* srow = reinterpret_cast<int*>(smem + SM::kRowOffset);
   int* spos = reinterpret_cast<int*>(smem + SM::kPosOffset);
 
-  // announce this CTA to its cluster (the partial exchange waits for it)
-  cluster_arrive_relaxed();
+  // announce this CTA to its cluster (the partial exchange waits for it);
+  // a single split has no partner and skips every cluster barrier
+  if (p.splits > 1) cluster_arrive_relaxed();
 
   int bad = 0;
   CtaList c = make_cta_list<MODE>(p, b, split, bad);
@@ -908,7 +910,8 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
     for (int w = 0; w < kWarps; ++w) sc[w] = fast_exp2(wm[w * kSlots + h] - base);
     return M;
   };
-  cluster_wait();   // every CTA of the cluster has started (its receive area exists)
+  const bool solo = S == 1;   // own shared memory, a CTA barrier instead of the cluster's
+  if (!solo) cluster_wait();   // every CTA of the cluster has started (its receive area exists)
   for (int e = tid; e < S * kSlots; e += kThreads) {
     const int r = e / kSlots, h = e % kSlots;
     float sc[kWarps];
@@ -916,7 +919,10 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
     float L = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) L = fmaf(wl[w * kSlots + h], sc[w], L);
-    st_dsmem_f32x2(rml + (rank * kSlots + h) * 2, r, M, L);
+    if (solo)
+      *reinterpret_cast<float2*>(rml + h * 2) = make_float2(M, L);
+    else
+      st_dsmem_f32x2(rml + (rank * kSlots + h) * 2, r, M, L);
   }
   for (int e = tid; e < n_pairs; e += kThreads) {
     const int h = e / C4, c4 = e % C4;
@@ -932,9 +938,15 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
       a.w = fmaf(v.w, sc[w], a.w);
     }
     const int r = e / per;
-    st_dsmem_f32x4(racc + ((size_t)rank * per + (e - r * per)) * 4, r, a);
+    if (solo)
+      *reinterpret_cast<float4*>(racc + (size_t)e * 4) = a;
+    else
+      st_dsmem_f32x4(racc + ((size_t)rank * per + (e - r * per)) * 4, r, a);
   }
-  cluster_sync();   // release the pushes, acquire everyone else's
+  if (solo)
+    __syncthreads();
+  else
+    cluster_sync();   // release the pushes, acquire everyone else's
 
   // ---------------- owner: merge the S partials of its pairs (local memory only)
   // Each thread forms its head's max and 1/sum over the S partials itself
