@@ -652,6 +652,92 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
     voff[q] = vr * ROWB + ((vc ^ (vr & 7)) << 4);
   }
 
+  // Tensor-core tile body, in two parts so that the next tile's QK^T can be
+  // issued before this tile's softmax and PV (software pipelining).
+  // (1) S^T of the tile whose K rows start at shared address kA.
+  auto tile_qk = [&](uint32_t kA, float cfr[4]) {
+    // S^T[16 keys x 8 heads] = K[16 x D] . Q^T[D x 8] in kChains independent
+    // accumulation chains (16-wide slices of d taken round robin) to cut
+    // the dependent MMA latency
+    constexpr int kChains = D / 16 >= 4 ? 4 : D / 16;
+    float cc[kChains][4];
+#pragma unroll
+    for (int q = 0; q < kChains; ++q) cc[q][0] = cc[q][1] = cc[q][2] = cc[q][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      // chunk 2ks + (lane >> 4) of row `lane & 15`, swizzled: a lane
+      // constant for ks % 4 plus 8 chunks per 4 ks
+      uint32_t a[4];
+      ldmatrix_x4(a, kA + koff[ks & 3] + (ks >> 2) * 128);
+      mma_bf16(cc[ks % kChains], a, sm_.qf[ks][0], sm_.qf[ks][1]);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float s = cc[0][e];
+#pragma unroll
+      for (int q = 1; q < kChains; ++q) s += cc[q][e];
+      cfr[e] = s;
+    }
+  };
+  // (2) masks, logits (focal), online softmax and O^T += V^T P^T for the tile
+  // of work-list entries [tbase, tbase + 16) whose V rows start at vA.
+  auto tile_rest = [&](const float cfr[4], uint32_t vA, int tbase, int n_round) {
+    // cache positions of keys gid and gid+8 (-1: masked or past the end)
+    const int posA = tbase + gid < n_round ? spos[tbase + gid] : -1;
+    const int posB = tbase + gid + 8 < n_round ? spos[tbase + gid + 8] : -1;
+    const float s0 = posA >= 0 ? cfr[0] * p.scale_log2 : kNegInf;
+    const float s1 = posA >= 0 ? cfr[1] * p.scale_log2 : kNegInf;
+    const float s2 = posB >= 0 ? cfr[2] * p.scale_log2 : kNegInf;
+    const float s3 = posB >= 0 ? cfr[3] * p.scale_log2 : kNegInf;
+    if (MODE == kFocal) {
+      if (posA >= c.img_start && posA < c.img_start + c.n_img)
+        *reinterpret_cast<float2*>(logit_base + (size_t)(posA - c.img_start) * kSlots + 2 * tig) =
+            make_float2(s0, s1);
+      if (posB >= c.img_start && posB < c.img_start + c.n_img)
+        *reinterpret_cast<float2*>(logit_base + (size_t)(posB - c.img_start) * kSlots + 2 * tig) =
+            make_float2(s2, s3);
+    }
+    // Online softmax with a lazily moved running max (base-2 logits): the
+    // max and the output scale are updated only when a score exceeds the
+    // running max by more than kLazyMax, so most tiles need neither the
+    // cross-lane max nor a rescale; probabilities stay below 2^kLazyMax.
+    if (__any_sync(0xffffffffu, s0 > sm_.m[0] + kLazyMax || s2 > sm_.m[0] + kLazyMax ||
+                                    s1 > sm_.m[1] + kLazyMax || s3 > sm_.m[1] + kLazyMax)) {
+      const float mx0 = warp_max_gid(fmaxf(s0, s2));
+      const float mx1 = warp_max_gid(fmaxf(s1, s3));
+      const float mn0 = fmaxf(sm_.m[0], mx0), mn1 = fmaxf(sm_.m[1], mx1);
+      const float al0 = fast_exp2(sm_.m[0] - (mn0 == kNegInf ? 0.f : mn0));
+      const float al1 = fast_exp2(sm_.m[1] - (mn1 == kNegInf ? 0.f : mn1));
+      sm_.l[0] *= al0;
+      sm_.l[1] *= al1;
+      sm_.m[0] = mn0;
+      sm_.m[1] = mn1;
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) {
+        sm_.acc[mt][0] *= al0;
+        sm_.acc[mt][1] *= al1;
+        sm_.acc[mt][2] *= al0;
+        sm_.acc[mt][3] *= al1;
+      }
+    }
+    const float b0f = sm_.m[0] == kNegInf ? 0.f : sm_.m[0];
+    const float b1f = sm_.m[1] == kNegInf ? 0.f : sm_.m[1];
+    const float p0 = fast_exp2(s0 - b0f), p2 = fast_exp2(s2 - b0f);
+    const float p1 = fast_exp2(s1 - b1f), p3 = fast_exp2(s3 - b1f);
+    sm_.l[0] += p0 + p2;
+    sm_.l[1] += p1 + p3;
+    // P^T[16 keys x 8 heads] as the B operand: transpose the two 8x8 blocks
+    const uint32_t bb0 = movmatrix_trans(pack_bf16(p0, p1));
+    const uint32_t bb1 = movmatrix_trans(pack_bf16(p2, p3));
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      uint32_t a[4];
+      ldmatrix_x4_trans(a, vA + voff[mt & 3] + (mt >> 2) * 128);
+      // O^T[16 dims x 8 heads] += V^T[16 dims x 16 keys] . P^T[16 keys x 8 heads]
+      mma_bf16(sm_.acc[mt], a, bb0, bb1);
+    }
+  };
+
   // ---------------- stream the work list in rounds of kSliceMax entries
   for (int rb = 0; rb < n_cta; rb += kSliceMax) {
     const int n_round = min(n_cta - rb, kSliceMax);
@@ -670,6 +756,32 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
       if (j < my_tiles) issue(j, n_round);
       cp_async_commit();
     }
+    if constexpr (kMma && ST >= 4) {
+      // Software pipelined (deep variant): the next tile's QK^T is issued
+      // before this tile's softmax and PV, keeping ST-2 tiles in flight.
+      // Tile j of this warp sits in stage j % ST and in commit group j, or
+      // j + 1 once all ST stages were staged before the wait (`first` == ST,
+      // an empty group follows them): wait<ST-2> covers the next tile in both.
+      float cfr_n[4];
+      if (my_tiles > 0) {
+        cp_async_wait<ST - 2>();
+        __syncwarp();
+        tile_qk(smem_u32(pipe), cfr_n);
+      }
+      for (int it = 0; it < my_tiles; ++it) {
+        const int jn = it + ST - 1;   // tiles below `first` were staged already
+        if (jn >= first && jn < my_tiles) issue(jn, n_round);
+        cp_async_commit();
+        const float cfr[4] = {cfr_n[0], cfr_n[1], cfr_n[2], cfr_n[3]};
+        cp_async_wait<ST - 2>();
+        __syncwarp();
+        // past the last tile this reads a stage no copy is writing; unused
+        tile_qk(smem_u32(pipe + ((it + 1) % ST) * SM::kStageBytes), cfr_n);
+        tile_rest(cfr, smem_u32(pipe + (it % ST) * SM::kStageBytes + kTile * ROWB),
+                  (warp + it * kWarps) * kTile, n_round);
+        __syncwarp();
+      }
+    } else {
     for (int it = 0; it < my_tiles; ++it) {
       const int jn = it + ST - 1;   // tiles below `first` were staged already
       if (jn >= first && jn < my_tiles) issue(jn, n_round);
@@ -682,84 +794,9 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
       const int tbase = (warp + it * kWarps) * kTile;   // tile start within the round
 
       if constexpr (kMma) {
-        // S^T[16 keys x 8 heads] = K[16 x D] . Q^T[D x 8] in kChains independent
-        // accumulation chains (16-wide slices of d taken round robin) to cut
-        // the dependent MMA latency
-        constexpr int kChains = D / 16 >= 4 ? 4 : D / 16;
-        float cc[kChains][4];
-#pragma unroll
-        for (int q = 0; q < kChains; ++q) cc[q][0] = cc[q][1] = cc[q][2] = cc[q][3] = 0.f;
-        const uint32_t kA = smem_u32(kS), vA = smem_u32(vS);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          // chunk 2ks + (lane >> 4) of row `lane & 15`, swizzled: a lane
-          // constant for ks % 4 plus 8 chunks per 4 ks
-          uint32_t a[4];
-          ldmatrix_x4(a, kA + koff[ks & 3] + (ks >> 2) * 128);
-          mma_bf16(cc[ks % kChains], a, sm_.qf[ks][0], sm_.qf[ks][1]);
-        }
         float cfr[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float s = cc[0][e];
-#pragma unroll
-          for (int q = 1; q < kChains; ++q) s += cc[q][e];
-          cfr[e] = s;
-        }
-        // cache positions of keys gid and gid+8 (-1: masked or past the end)
-        const int posA = tbase + gid < n_round ? spos[tbase + gid] : -1;
-        const int posB = tbase + gid + 8 < n_round ? spos[tbase + gid + 8] : -1;
-        const float s0 = posA >= 0 ? cfr[0] * p.scale_log2 : kNegInf;
-        const float s1 = posA >= 0 ? cfr[1] * p.scale_log2 : kNegInf;
-        const float s2 = posB >= 0 ? cfr[2] * p.scale_log2 : kNegInf;
-        const float s3 = posB >= 0 ? cfr[3] * p.scale_log2 : kNegInf;
-        if (MODE == kFocal) {
-          if (posA >= c.img_start && posA < c.img_start + c.n_img)
-            *reinterpret_cast<float2*>(logit_base + (size_t)(posA - c.img_start) * kSlots + 2 * tig) =
-                make_float2(s0, s1);
-          if (posB >= c.img_start && posB < c.img_start + c.n_img)
-            *reinterpret_cast<float2*>(logit_base + (size_t)(posB - c.img_start) * kSlots + 2 * tig) =
-                make_float2(s2, s3);
-        }
-        // Online softmax with a lazily moved running max (base-2 logits): the
-        // max and the output scale are updated only when a score exceeds the
-        // running max by more than kLazyMax, so most tiles need neither the
-        // cross-lane max nor a rescale; probabilities stay below 2^kLazyMax.
-        if (__any_sync(0xffffffffu, s0 > sm_.m[0] + kLazyMax || s2 > sm_.m[0] + kLazyMax ||
-                                        s1 > sm_.m[1] + kLazyMax || s3 > sm_.m[1] + kLazyMax)) {
-          const float mx0 = warp_max_gid(fmaxf(s0, s2));
-          const float mx1 = warp_max_gid(fmaxf(s1, s3));
-          const float mn0 = fmaxf(sm_.m[0], mx0), mn1 = fmaxf(sm_.m[1], mx1);
-          const float al0 = fast_exp2(sm_.m[0] - (mn0 == kNegInf ? 0.f : mn0));
-          const float al1 = fast_exp2(sm_.m[1] - (mn1 == kNegInf ? 0.f : mn1));
-          sm_.l[0] *= al0;
-          sm_.l[1] *= al1;
-          sm_.m[0] = mn0;
-          sm_.m[1] = mn1;
-#pragma unroll
-          for (int mt = 0; mt < D / 16; ++mt) {
-            sm_.acc[mt][0] *= al0;
-            sm_.acc[mt][1] *= al1;
-            sm_.acc[mt][2] *= al0;
-            sm_.acc[mt][3] *= al1;
-          }
-        }
-        const float b0f = sm_.m[0] == kNegInf ? 0.f : sm_.m[0];
-        const float b1f = sm_.m[1] == kNegInf ? 0.f : sm_.m[1];
-        const float p0 = fast_exp2(s0 - b0f), p2 = fast_exp2(s2 - b0f);
-        const float p1 = fast_exp2(s1 - b1f), p3 = fast_exp2(s3 - b1f);
-        sm_.l[0] += p0 + p2;
-        sm_.l[1] += p1 + p3;
-        // P^T[16 keys x 8 heads] as the B operand: transpose the two 8x8 blocks
-        const uint32_t bb0 = movmatrix_trans(pack_bf16(p0, p1));
-        const uint32_t bb1 = movmatrix_trans(pack_bf16(p2, p3));
-#pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-          uint32_t a[4];
-          ldmatrix_x4_trans(a, vA + voff[mt & 3] + (mt >> 2) * 128);
-          // O^T[16 dims x 8 heads] += V^T[16 dims x 16 keys] . P^T[16 keys x 8 heads]
-          mma_bf16(sm_.acc[mt], a, bb0, bb1);
-        }
+        tile_qk(smem_u32(kS), cfr);
+        tile_rest(cfr, smem_u32(vS), tbase, n_round);
       } else {
         const float* qs = reinterpret_cast<const float*>(smem + SM::kQOffset);
         const int r = lane & 15, half = lane >> 4;
@@ -825,6 +862,7 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
         }
       }
       __syncwarp();
+    }
     }
     cp_async_wait<0>();
     __syncthreads();   // before the next round overwrites the row list

@@ -328,29 +328,6 @@ __device__ __forceinline__ float warp_sum_gid(float x) {
   return x;
 }
 
-// Exclusive prefix sum over the CTA (kThreads threads); `scratch` holds kWarps ints.
-__device__ __forceinline__ int block_exclusive_scan(int x, int* scratch, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = x;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  __syncthreads();
-  if (lane == 31) scratch[warp] = incl;
-  __syncthreads();
-  int before = 0, all = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    int v = scratch[w];
-    if (w < warp) before += v;
-    all += v;
-  }
-  if (total) *total = all;
-  return before + incl - x;
-}
-
 // ---------------------------------------------------------------- per-warp state
 
 // bf16 tensor-core path: thread (gid = lane/4, tig = lane%4) owns query-head
