@@ -525,11 +525,19 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
     }
   }
   const int n_pre = min(kSliceMax, n_txt_pad + n_sel_pad);   // entries before the current token
+  // q and the current token's K/V may still be written by the previous
+  // kernel, so they are read only after the wait; pulling their lines into L2
+  // now is safe (L2 is where those writes land) and shortens that read.
+  if (tid == 0)
+    prefetch_l2(static_cast<const T*>(p.q) + ((size_t)b * p.Hq + (size_t)hkv * p.g) * D,
+                p.g * D * (uint32_t)sizeof(T));
   if (c.has_cur && tid == 0 && n_pre < kSliceMax) {
     const int page = __ldcg(bt + (c.cur_pos >> p.log2_page));
     int row = -1, ps = c.cur_pos;
     if (page >= 0 && page < p.num_pages) {
       row = ((page * p.Hkv + hkv) << p.log2_page) | (ps & page_mask);
+      prefetch_l2(kg + (size_t)row * D, ROWB);
+      prefetch_l2(vg + (size_t)row * D, ROWB);
     } else {
       bad |= kDevBadPage;
       ps = -1;
