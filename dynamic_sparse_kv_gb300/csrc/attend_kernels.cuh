@@ -284,14 +284,14 @@ constexpr bool deep_fits() {
 // of len/S tokens at ~8 ns per token when it runs alone, slowed down when a
 // wave of CTAs together asks for more than HBM delivers (~40 GB/s per CTA
 // under load); clusters run in waves of active[S]; every doubling of the
-// cluster adds ~0.35 us of merge and barrier latency; a grid of at most
+// cluster adds ~0.25 us of merge and barrier latency; a grid of at most
 // num_sms CTAs also lets the next kernel's CTAs stage their first tiles
 // while it runs (programmatic dependent launch), worth ~1.5 us. Fitted to
-// graph-replayed decode steps on GB300 (1 sequence: 4-6 splits for gather
+// graph-replayed decode steps on GB300 (1 sequence: ~6 splits for gather
 // layers, 16 for full ones; 32 sequences: 1 and 2; 8 sequences of 16k
 // image tokens: 4 for gather layers).
 inline int choose_splits(long units, long len, int max_splits, const int* active, int num_sms) {
-  const double ns_per_token = 8.0, cta_gbs = 40.0, hbm_gbs = 6500.0, us_per_doubling = 0.35,
+  const double ns_per_token = 8.0, cta_gbs = 40.0, hbm_gbs = 6500.0, us_per_doubling = 0.25,
                overlap_us = 1.5;
   if (len < 1) len = 1;
   int best = 1;
