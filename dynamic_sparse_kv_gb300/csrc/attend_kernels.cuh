@@ -9,20 +9,23 @@
 //            (FastOCR, cross-layer propagation / Cross-Step Fixation Reuse)
 //   rswa   : [0, L_m) ++ [max(L_m, N_t - n), N_t)           (Unlimited OCR, R-SWA)
 //
-// Work decomposition (split-K flash-decode): grid = (splits, H_kv, B). A CTA
-// owns one KV head of one sequence and a contiguous slice of the attend list;
-// its four warps stream 16-token tiles of that slice independently through a
-// 3-stage cp.async pipeline (16-byte chunks, XOR-swizzled rows, so any
-// gathered row is a coalesced 256-byte read and ldmatrix is conflict-free).
-// For bf16 the GQA group (g <= 8 query heads) x 16 keys contraction and the
-// P.V product run on the tensor cores (mma.sync m16n8k16, keys/head-dim on M,
-// query heads on N); fp32 runs on the CUDA cores. Softmax is online in the
-// base-2 domain. The last CTA to finish a (sequence, KV head) merges the
-// split partials (no spin-waits: an atomic ticket decides who merges). In
-// focal mode that CTA also turns its group's logits into probabilities
-// summed over its query heads, and the last KV-head CTA of the sequence sums
-// the groups and runs a radix select for the top k (ties to the lower
-// position), writing the selection without a host round trip.
+// Work decomposition (split-K flash-decode): grid = (splits, H_kv, B); the S
+// splits of one (sequence, KV head) form a thread-block cluster. A CTA owns a
+// contiguous slice of that KV head's attend list; its four warps stream
+// 16-token tiles of the slice independently through a cp.async pipeline (3
+// stages; 6 for grids that leave every CTA an SM of its own), in 16-byte
+// chunks into XOR-swizzled rows, so any gathered row is a coalesced 256-byte
+// read and ldmatrix is conflict-free. For bf16 the GQA group (g <= 8 query
+// heads) x 16 keys contraction and the P.V product run on the tensor cores
+// (mma.sync m16n8k16, keys / head dims on M, query heads on N); fp32 runs on
+// the CUDA cores. Softmax is online in the base-2 domain with a lazily moved
+// running max. The CTAs of a cluster push their partials into each other's
+// shared memory and merge after one cluster barrier (no global partials, no
+// spin-waits). In focal mode every CTA also stores its image tokens' logits
+// and, after the merge, turns them into its KV head's share of the head-summed
+// probabilities; a separate one-CTA-per-sequence kernel, chained by
+// programmatic dependent launch, sums the KV heads and radix-selects the top
+// k (ties to the lower position) without a host round trip.
 #pragma once
 
 #include <cuda_bf16.h>
