@@ -126,8 +126,9 @@ int32_t fastocr_abi_version(void);
 const char* fastocr_status_string(int32_t status);
 
 /* Create a handle for the current CUDA device: checks dims, allocates the
- * workspace (split partials, focal logits, scores, counters, profiler
- * accumulator, device status word) once. *out is set only on FASTOCR_OK.
+ * workspace (focal-layer image logits, per-KV-head image scores, profiler
+ * accumulator, device status word) once; split partials never leave the
+ * chip (they merge in distributed shared memory). *out is set only on FASTOCR_OK.
  * Synchronous. Errors: NULL, INVALID, UNSUPPORTED, NO_DEVICE, CUDA. */
 fastocr_status fastocr_create(const fastocr_dims* dims, fastocr_handle** out);
 
