@@ -26,6 +26,14 @@ Readings (each pinned by a test):
 * a step with no F_last yet (no warm-up and step 0) runs the layers before the
   first focal layer on the full cache;
 * selections are per sequence and shared by all heads of all non-focal layers.
+
+Adaptive layer selection (named by both summaries' closing section as a
+future direction, with no rule given): the plainest form is taken -- the
+warm-up profile is re-run for the same w steps every `period` steps (steps
+[m*period, m*period + w)), each window's ratio starts from zero, and at the
+window's end C is chosen anew and F_last restarts from the new deepest focal
+layer's selection, exactly as after the first warm-up. period None is the
+published method (one window).
 """
 from __future__ import annotations
 
@@ -99,31 +107,54 @@ def steady_step(q_step, kv, n_t, img, tau, focal, f_last, accept=None):
     return outs, used, list(current)
 
 
+def window_position(t: int, warmup: int, period=None) -> int:
+    """Position of decode step t in its profiling window, -1 for a steady step.
+    Windows are [0, warmup) (period None) or [m*period, m*period + warmup)."""
+    pos = t if period is None else t % period
+    return pos if pos < warmup else -1
+
+
+def accumulate_ratio(ratio, mass, pos: int, warmup: int, batch: int, n_q: int):
+    """The window's image-attention ratio after its profiling step at window
+    position pos: a window starts from zero; each step adds its image mass
+    averaged over the window's steps, the sequences and the query heads."""
+    base = ratio if pos > 0 else np.zeros_like(ratio)
+    return base + mass / (warmup * batch * n_q)
+
+
 def run_decode(q_of, kv_of, n_t_of, img, tau, n_layers, batch, n_q, steps, warmup=0,
-               n_focal=3, focal_layers=None, accept=None):
+               n_focal=3, focal_layers=None, accept=None, period=None):
     """Whole schedule over decode steps 0 .. steps-1.
 
     q_of(t) -> [L, B, H_q, d]; kv_of(t) -> kv(layer, b); n_t_of(t) -> [B];
-    accept(t, l, b, selection, sigma) as in steady_step.
-    Returns dict(outs=[steps] arrays, used=[steps][L][B], focal=C, ratio=[L])."""
+    accept(t, l, b, selection, sigma) as in steady_step; period: re-profile
+    every `period` steps (adaptive layer selection), None: profile once.
+    Returns dict(outs=[steps] arrays, used=[steps][L][B], focal=C (the last
+    chosen), ratio=[L] (of the last window), f_last, focal_history=[(step at
+    which a window ended, C chosen)])."""
+    if period is not None and period <= warmup:
+        raise ValueError("period must exceed the profiling window")
     ratio = np.zeros(n_layers)
     focal = tuple(focal_layers) if focal_layers is not None else None
     f_last = [None] * batch
-    outs, used = [], []
+    outs, used, history = [], [], []
     for t in range(steps):
         q_step, kv, n_t = q_of(t), kv_of(t), n_t_of(t)
         acc = (lambda l, b, s, sg, t=t: accept(t, l, b, s, sg)) if accept else None
-        if t < warmup:
+        pos = window_position(t, warmup, period)
+        if pos >= 0:
             o, mass, sel = warmup_step(q_step, kv, n_t, img, tau, acc)
-            ratio += mass / (warmup * batch * n_q)
+            ratio = accumulate_ratio(ratio, mass, pos, warmup, batch, n_q)
             outs.append(o)
             used.append([[None] * batch for _ in range(n_layers)])
-            if t == warmup - 1:
-                if focal is None:
+            if pos == warmup - 1:
+                if focal_layers is None:
                     focal = choose_focal_layers(ratio, n_focal)
                 f_last = list(sel[max(focal)])
+                history.append((t, focal))
         else:
             o, u, f_last = steady_step(q_step, kv, n_t, img, tau, focal, f_last, acc)
             outs.append(o)
             used.append(u)
-    return dict(outs=outs, used=used, focal=focal, ratio=ratio, f_last=f_last)
+    return dict(outs=outs, used=used, focal=focal, ratio=ratio, f_last=f_last,
+                focal_history=history)

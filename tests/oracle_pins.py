@@ -348,9 +348,72 @@ def pin_warmup_profile():
     np.testing.assert_allclose(out0, want, rtol=1e-12, atol=1e-13)
 
 
+def pin_reprofile_windows():
+    """Adaptive layer selection: a second profiling window re-chooses C from its
+    own steps only (the first window's mass is not carried over) and F_last
+    restarts from the new deepest focal layer's last-window selection; steady
+    steps between the windows keep the first C."""
+    rng = _rng(23)
+    n_layers, n_q, n_kv, d = 6, 4, 2, 16
+    P, n_img, w, period, steps = 4, 16, 2, 5, 9
+    # window 1 pulls layers 0, 1, 3 to the image and pushes 2, 4, 5 away;
+    # window 2 pulls 2, 4, 5 a little harder than 0, 1, 3 -- so the mass of
+    # both windows together would still rank 0, 1, 3 first
+    beta_1 = [3.0, 3.0, -3.0, 3.0, -3.0, -3.0]
+    beta_2 = [1.0, 1.0, 2.0, 1.0, 2.0, 2.0]
+    n_max = P + n_img + steps
+    Ks = [0.1 * rng.standard_normal((n_max, n_kv, d)) for _ in range(n_layers)]
+    for K in Ks:
+        K[P:P + n_img, :, 0] += 1.0                    # image keys share direction e_0
+    Vs = [rng.standard_normal((n_max, n_kv, d)) for _ in range(n_layers)]
+    qs = []
+    for t in range(steps):
+        beta = beta_1 if t < period else beta_2
+        q = 0.05 * rng.standard_normal((n_layers, 1, n_q, d))
+        for l in range(n_layers):
+            q[l, 0, :, 0] += beta[l] * math.sqrt(d)
+        qs.append(q)
+    kv_of = lambda t: (lambda l, b: (Ks[l], Vs[l]))  # noqa: E731
+    n_t_of = lambda t: np.array([P + n_img + t + 1])  # noqa: E731
+    img = np.array([[P, n_img]])
+    res = S.run_decode(lambda t: qs[t], kv_of, n_t_of, img, 0.25, n_layers, 1, n_q, steps,
+                       warmup=w, n_focal=3, period=period)
+    assert res["focal_history"] == [(w - 1, (0, 1, 3)), (period + w - 1, (2, 4, 5))], \
+        res["focal_history"]
+
+    def sel_of(t, l):
+        return A.focal_attend(qs[t][l, 0], Ks[l], Vs[l], P + n_img + t + 1, P, n_img, 0.25)[1]
+
+    def sparse(t, l, sel):
+        return A.sparse_attend(qs[t][l, 0], Ks[l], Vs[l], P + n_img + t + 1, P, n_img, sel)
+
+    # window 2 runs full attention everywhere
+    t2 = period
+    for l in range(n_layers):
+        np.testing.assert_allclose(res["outs"][t2][l, 0],
+                                   A.full_attend(qs[t2][l, 0], Ks[l], Vs[l], P + n_img + t2 + 1),
+                                   rtol=1e-12, atol=1e-13)
+    # a steady step between the windows runs C = (0, 1, 3): layer 2 reads layer 1's selection
+    t1 = period - 1
+    np.testing.assert_allclose(res["outs"][t1][2, 0], sparse(t1, 2, sel_of(t1, 1)),
+                               rtol=1e-12, atol=1e-13)
+    # the first step after window 2 runs C = (2, 4, 5): layers 0 and 1 read F_last,
+    # layer 5's selection in the window's last step; layer 3 reads layer 2's
+    t3 = period + w
+    for l in (0, 1):
+        np.testing.assert_allclose(res["outs"][t3][l, 0], sparse(t3, l, sel_of(t3 - 1, 5)),
+                                   rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(res["outs"][t3][3, 0], sparse(t3, 3, sel_of(t3, 2)),
+                               rtol=1e-12, atol=1e-13)
+    # no period: one window, the first C for good
+    once = S.run_decode(lambda t: qs[t], kv_of, n_t_of, img, 0.25, n_layers, 1, n_q, steps,
+                        warmup=w, n_focal=3)
+    assert once["focal_history"] == [(w - 1, (0, 1, 3))]
+
+
 ALL_PINS = [
     pin_attend_matches_sdpa, pin_attend_closed_forms, pin_gather_order_invariant,
     pin_select_exhaustive, pin_keep_counts, pin_image_scores, pin_tau_one_is_full,
     pin_attend_sets_golden, pin_rswa_short_is_full, pin_focal_layer_choice,
-    pin_cross_step_reuse, pin_warmup_profile,
+    pin_cross_step_reuse, pin_warmup_profile, pin_reprofile_windows,
 ]

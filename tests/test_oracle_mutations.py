@@ -109,6 +109,16 @@ def _steady_first_focal_only(q_step, kv, n_t, img, tau, focal, f_last, accept=No
     return outs, used, list(current)
 
 
+def _accumulate_no_reset(ratio, mass, pos, warmup, batch, n_q):
+    # mistake: a new profiling window keeps the previous window's mass
+    return ratio + mass / (warmup * batch * n_q)
+
+
+def _window_never_repeats(t, warmup, period=None):
+    # mistake: the period is ignored, so the profile runs only once
+    return t if t < warmup else -1
+
+
 MUTATIONS = {
     "gqa_modulo": (A, "attend", _attend_variant(gqa="mod")),
     "scale_1_over_d": (A, "attend", _attend_variant(scale="d")),
@@ -123,6 +133,8 @@ MUTATIONS = {
     "rswa_without_current": (A, "rswa_positions", _rswa_without_current),
     "focal_choice_lowest": (S, "choose_focal_layers", _choose_lowest),
     "first_focal_not_replaced": (S, "steady_step", _steady_first_focal_only),
+    "reprofile_keeps_old_mass": (S, "accumulate_ratio", _accumulate_no_reset),
+    "reprofile_never_repeats": (S, "window_position", _window_never_repeats),
 }
 
 
