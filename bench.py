@@ -18,6 +18,7 @@ sequences, seed + rank); value = all ranks' steps / max-over-ranks time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -50,6 +51,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-compare", action="store_true", help="skip the dense / tau=1 arms")
+    ap.add_argument("--rswa-ring", action="store_true",
+                    help="R-SWA: keep only prefix + window pages per sequence (ring block table)")
     ap.add_argument("--oracle-leg", default=None, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
@@ -175,8 +178,11 @@ def oracle_leg(spec: str):
     # the sample: every layer of sequence 0, decode steps after warm-up, until
     # the time budget is used (at least 2 steps)
     wl1 = wl.with_(batch=1)
-    max_steps = min(wl1.steps, wl1.warmup + 64)
-    case = synth.make_case(wl1, device="cpu", n_steps=max_steps)
+    if wl1.mode == "rswa":   # the late steps the GPU bench times (window full)
+        t_first, max_steps = max(0, wl1.steps - 64), wl1.steps
+    else:
+        t_first, max_steps = 0, min(wl1.steps, wl1.warmup + 64)
+    case = synth.make_case(wl1, device="cpu", step0=t_first, n_steps=max_steps - t_first)
     kvs = {}
 
     def kv(l, b):
@@ -189,7 +195,7 @@ def oracle_leg(spec: str):
     for l in range(wl1.layers):
         kv(l, 0)
     focal, f_last = wl1.focal_layers, [None]
-    t = 0
+    t = t_first
     if wl1.mode == "fastocr" and focal is None:
         ratio = np.zeros(wl1.layers)
         for t in range(wl1.warmup):
@@ -269,13 +275,30 @@ def run_gpu(args, rank, world, local_rank):
     wl = wl.with_(seed=wl.seed + 1000 * rank)
     K, W = args.steps, args.warmup
     assert W >= 3, "at least 3 warm-up steps"
-    t0_steady = wl.warmup if wl.mode == "fastocr" else 0
+    if wl.mode == "fastocr":
+        t0_steady, step0 = wl.warmup, 0         # the warm-up reads steps [0, warmup)
+    else:   # R-SWA: the last steps before T = wl.steps generated tokens (window full)
+        t0_steady = step0 = max(0, wl.steps - (W + K))
     span = wl.steps - t0_steady                 # steady steps available in the workload
-    n_gen = min(wl.steps, t0_steady + W + K)
-    case = synth.make_case(wl, device=dev, n_steps=n_gen)
+    n_gen = min(wl.steps, t0_steady + W + K) - step0
+    case = synth.make_case(wl, device=dev, step0=step0, n_steps=n_gen)
+    storage = "full"
+    if wl.mode == "rswa" and args.rswa_ring:
+        # bounded memory: pages past the prefix form a ring of ceil(n / page)
+        # pages per sequence; the timed kernels are the same
+        from dynamic_sparse_kv_gb300 import ring_block_table
+        table, per = ring_block_table(wl.batch, wl.rswa_prefix, wl.rswa_window, wl.page_size,
+                                      wl.max_tokens)
+        n_pages = wl.batch * per
+        k_ring = case.k_cache[:, :n_pages].clone()
+        v_ring = case.v_cache[:, :n_pages].clone()
+        case = dataclasses.replace(case, k_cache=k_ring, v_cache=v_ring,
+                                   block_table=table.to(dev))
+        torch.cuda.empty_cache()
+        storage = "ring"
 
     def t_of(i):                                # i-th bench step -> decode step index
-        return t0_steady + (i % min(span, n_gen - t0_steady))
+        return t0_steady + (i % min(span, n_gen - (t0_steady - step0)))
 
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
@@ -395,16 +418,6 @@ def run_gpu(args, rank, world, local_rank):
                 if peak_src == "measured" else "fallback 6.8 TB/s",
                 "traffic": recorded_traffic(kname, wl.name)}
 
-    # ---- comparison arms: dense (every layer full) and the tau = 1 FastOCR pipeline
-    compare = {}
-    if not args.no_compare and kind == "fastocr":
-        dcap = CapturedStep(dec, "dense")
-        per_d, _, _ = time_graph(dec, dcap, W, min(K, 200))
-        compare["dense_us_per_step"] = statistics.fmean(per_d) * 1e3
-        dec1, _, cap1 = build(1.0, "fastocr")
-        per_1, _, _ = time_graph(dec1, cap1, W, min(K, 200))
-        compare["tau1_us_per_step"] = statistics.fmean(per_1) * 1e3
-        dec1.close()
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -431,6 +444,30 @@ def run_gpu(args, rank, world, local_rank):
         e2e = {"value": world * n_e / (e_ms * 1e-3), "unit": "steps/s",
                "h2d_bytes_per_step": qb, "d2h_bytes_per_step": cap.out.numel() * cap.out.element_size(),
                "us_per_step": e_ms * 1e3 / n_e}
+
+    # ---- comparison arms: dense (every layer full) and the tau = 1 FastOCR pipeline
+    compare = {}
+    if not args.no_compare and kind == "fastocr":
+        dcap = CapturedStep(dec, "dense")
+        per_d, _, _ = time_graph(dec, dcap, W, min(K, 200))
+        compare["dense_us_per_step"] = statistics.fmean(per_d) * 1e3
+        dec1, _, cap1 = build(1.0, "fastocr")
+        per_1, _, _ = time_graph(dec1, cap1, W, min(K, 200))
+        compare["tau1_us_per_step"] = statistics.fmean(per_1) * 1e3
+        dec1.close()
+        # adaptive layer selection: the cost of one profiling step (full
+        # attention, scoring, selection and profile accumulation in every
+        # layer) and of capturing the steady step anew after C changes
+        pcap = CapturedStep(dec, "profile")
+        per_p, _, _ = time_graph(dec, pcap, W, min(K, 200))
+        compare["profile_us_per_step"] = statistics.fmean(per_p) * 1e3
+        torch.cuda.synchronize()
+        c0 = time.perf_counter()
+        del pcap
+        pcap = CapturedStep(dec, "fastocr")
+        torch.cuda.synchronize()
+        compare["recapture_ms"] = (time.perf_counter() - c0) * 1e3
+        del pcap
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -464,6 +501,11 @@ def run_gpu(args, rank, world, local_rank):
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": cap.launches * K, "clocks": clocks,
     }
+    if wl.mode == "rswa":
+        res["config"].update({
+            "rswa_prefix": wl.rswa_prefix, "rswa_window": wl.rswa_window,
+            "generated_tokens_timed": [t_of(W) + 1, t_of(W + K - 1) + 1], "storage": storage,
+            "kv_cache_bytes_per_layer": 2 * case.k_cache[0].numel() * case.k_cache.element_size()})
     if "dense_us_per_step" in compare:
         res["config"]["speedup_vs_dense"] = compare["dense_us_per_step"] / us_per_step
         res["config"]["speedup_vs_tau1"] = compare["tau1_us_per_step"] / us_per_step

@@ -12,4 +12,5 @@ from ._native import (  # noqa: F401
     fastocr_focal_attend, fastocr_full_attend, fastocr_profiler_reset, fastocr_profiler_select,
     fastocr_rswa_attend, fastocr_set_length_hint, fastocr_set_splits, fastocr_sparse_attend,
     make_kv)
-from .decoder import CapturedStep, DecodeAttention, keep_capacity, ring_block_table  # noqa: F401
+from .decoder import (CapturedStep, DecodeAttention, ProfileSchedule, keep_capacity,  # noqa: F401
+                      ring_block_table)

@@ -62,6 +62,30 @@ def ring_block_table(batch: int, prefix_len: int, window: int, page_size: int, m
     return table.to(torch.int32), per
 
 
+class ProfileSchedule:
+    """Which decode steps profile the layers and which run the steady step.
+
+    A profiling step runs full attention in every layer and adds each layer's
+    image-attention mass to the profile; the last step of a window chooses the
+    focal set C and F_last (FastOCR, "Focal-Guided Pruning": focal layer
+    selection by a light warm-up). period None: one window, steps
+    [0, window) -- the published method. A period P > window re-runs the
+    window in steps [m*P, m*P + window) and re-chooses C each time, the
+    plainest form of the adaptive layer selection that the FastOCR summaries
+    name as future work; each window's profile starts from zero.
+    """
+
+    def __init__(self, window: int, period: int | None = None):
+        if window < 0 or (period is not None and period <= window):
+            raise ValueError("need 0 <= window < period")
+        self.window, self.period = int(window), period
+
+    def position(self, t: int) -> int:
+        """Position of step t in its profiling window, -1 for a steady step."""
+        pos = t if self.period is None else t % self.period
+        return pos if pos < self.window else -1
+
+
 class DecodeAttention:
     """Decode attention of a stack of layers over a paged KV cache.
 
@@ -156,6 +180,24 @@ class DecodeAttention:
         self.has_f_last = True
         return focal, mass
 
+    def scheduled_step(self, t: int, q, out, schedule: ProfileSchedule, n_focal: int,
+                       stream=None):
+        """Decode step t under `schedule`: a profiling step (the first of a window
+        resets the profile, the last chooses C and F_last, synchronising the
+        host) or the steady step. Returns C when this step chose it, else
+        None; a CapturedStep of the steady step must then be captured anew,
+        since it holds the previous focal layers."""
+        pos = schedule.position(t)
+        if pos < 0:
+            self.step(q, out, stream)
+            return None
+        if pos == 0:
+            self.begin_warmup(stream)
+        self.warmup_step(q, out, stream)
+        if pos == schedule.window - 1:
+            return self.finish_warmup(n_focal, stream)[0]
+        return None
+
     # ------------------------------------------------------------ steps
     def step(self, q, out, stream=None):
         """One steady FastOCR decode step over all layers (q, out: [L, B, H_q, d])."""
@@ -194,8 +236,9 @@ class CapturedStep:
 
     q, out: [L, B, H_q, d] device tensors owned by this object; write the
     step's queries into q (and N_t into dec.seq_len), then replay(). kind:
-    "fastocr" (steady FastOCR step), "dense" (full attention in every layer)
-    or "rswa".
+    "fastocr" (steady FastOCR step), "dense" (full attention in every layer),
+    "profile" (a profiling step: full attention with scoring, selection and
+    profile accumulation in every layer) or "rswa".
     """
 
     def __init__(self, dec: DecodeAttention, kind: str = "fastocr"):
@@ -203,7 +246,10 @@ class CapturedStep:
         shape = (dec.layers, dec.batch, dec.q_heads, dec.head_dim)
         self.q = torch.zeros(shape, dtype=dec.k_cache.dtype, device=dec.k_cache.device)
         self.out = torch.zeros_like(self.q)
-        fn = {"fastocr": dec.step, "dense": dec.dense_step, "rswa": dec.rswa_step}[kind]
+        if kind == "profile" and dec.warm_idx is None:
+            dec.begin_warmup()
+        fn = {"fastocr": dec.step, "dense": dec.dense_step, "rswa": dec.rswa_step,
+              "profile": dec.warmup_step}[kind]
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):

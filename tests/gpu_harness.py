@@ -82,11 +82,14 @@ def assert_close(gpu: torch.Tensor, ref: np.ndarray, tol: float, where=""):
 class GpuRun:
     """Run the CUDA path step by step, keeping outputs and selections on the host."""
 
-    def __init__(self, case, tau=None, focal_layers=None, splits=None):
-        from dynamic_sparse_kv_gb300 import DecodeAttention
+    def __init__(self, case, tau=None, focal_layers=None, splits=None, period=None):
+        from dynamic_sparse_kv_gb300 import DecodeAttention, ProfileSchedule
 
         wl = case.wl
         self.case, self.wl = case, wl
+        self.period = period
+        self.schedule = ProfileSchedule(wl.warmup, period)
+        self.focal_history = []
         self.tau = wl.tau if tau is None else tau
         self.focal_fixed = focal_layers if focal_layers is not None else wl.focal_layers
         self.dec = DecodeAttention(case.k_cache, case.v_cache, case.block_table,
@@ -116,14 +119,13 @@ class GpuRun:
                 dec.dense_step(q, out)
             elif kind == "rswa":
                 dec.rswa_step(q, out)
-            elif t < wl.warmup and self.focal_fixed is None:
-                if t == 0:
-                    dec.begin_warmup()
-                dec.warmup_step(q, out)
+            elif self.schedule.position(t) >= 0 and self.focal_fixed is None:
+                chosen = dec.scheduled_step(t, q, out, self.schedule, wl.n_focal)
                 self.sels[t] = self._selections(
                     {l: (dec.warm_idx[l], dec.warm_k[l]) for l in range(wl.layers)})
-                if t == wl.warmup - 1:
-                    self.focal, self.mass = dec.finish_warmup(wl.n_focal)
+                if chosen is not None:
+                    self.focal = tuple(chosen)
+                    self.focal_history.append((t, self.focal))
             else:
                 if self.focal is None:
                     self.focal = tuple(self.focal_fixed)
@@ -173,6 +175,12 @@ def compare_decode(run: GpuRun, steps: int, batch_idx=None, check_focal=True):
     common = (q_of, kv_of, n_t_of, img, run.tau, wl.layers, len(bsel), wl.q_heads, steps)
     if run.focal_fixed is not None:
         res = S.run_decode(*common, warmup=0, focal_layers=run.focal_fixed, accept=accept)
+    elif run.period is not None:
+        # re-profiled every run.period steps: every window's C must agree
+        res = S.run_decode(*common, warmup=wl.warmup, n_focal=wl.n_focal, accept=accept,
+                           period=run.period)
+        assert res["focal_history"] == run.focal_history, (res["focal_history"],
+                                                           run.focal_history)
     elif check_focal and len(bsel) == wl.batch:
         res = S.run_decode(*common, warmup=wl.warmup, n_focal=wl.n_focal, accept=accept)
         if tuple(res["focal"]) != tuple(run.focal):

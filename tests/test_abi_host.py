@@ -96,3 +96,19 @@ def test_header_compiles_as_c_and_cpp():
         r = subprocess.run([comp, "-fsyntax-only", "-Wall", "-Werror", "-x", lang, HEADER],
                            capture_output=True, text=True)
         assert r.returncode == 0, r.stderr
+
+
+def test_profile_schedule_windows(lib):
+    """The decoder's profiling windows are the oracle's: one window without a
+    period, a window of `window` steps at the start of every period with one."""
+    import oracle.schedule as S
+    from dynamic_sparse_kv_gb300 import ProfileSchedule
+    for window, period in [(8, None), (0, None), (2, 7), (3, 4), (1, 2), (0, 5)]:
+        sch = ProfileSchedule(window, period)
+        got = [sch.position(t) for t in range(40)]
+        assert got == [S.window_position(t, window, period) for t in range(40)]
+    assert [ProfileSchedule(2, 7).position(t) for t in range(15)] == \
+        [0, 1, -1, -1, -1, -1, -1, 0, 1, -1, -1, -1, -1, -1, 0]
+    for bad in [(3, 3), (4, 2), (-1, None)]:
+        with pytest.raises(ValueError):
+            ProfileSchedule(*bad)

@@ -192,6 +192,84 @@ def test_large_and_rising_logits(pattern):
         assert_close(out_sparse[b], ref_sp, TOL["bf16"], f"sparse b={b}")
 
 
+def test_adaptive_reprofiling():
+    """Adaptive layer selection: the profile re-runs in 2-step windows every 7
+    steps; each window re-chooses C from its own steps and F_last restarts.
+    From the second window on, the first window's focal layers get queries
+    that seek the text prefix, so C must change. Every output, selection and
+    window's C matches the oracle's schedule with the same period."""
+    import oracle.schedule as S
+    from gpu_harness import oracle_inputs
+    case = _case("qwen7b_b1", batch=2, layers=6, prompt=24, grid=(1, 12, 16), steps=16,
+                 warmup=2, n_focal=2, tau=0.1)
+    wl = case.wl
+    period = 7
+    _, img, q_of, kv_of, n_t_of = oracle_inputs(case, KVCache(case))
+    first = S.run_decode(q_of, kv_of, n_t_of, img, wl.tau, wl.layers, wl.batch, wl.q_heads,
+                         wl.warmup, warmup=wl.warmup, n_focal=wl.n_focal)["focal"]
+    g = wl.q_heads // wl.kv_heads
+    for l in first:
+        for b in range(wl.batch):
+            K, _ = case.logical_kv(l, b, wl.prompt)           # [prompt, H_kv, d]
+            m = K.float().mean(0)
+            u = m / m.norm(dim=-1, keepdim=True)
+            case.q[period - case.step0:, l, b] = (40.0 * u).repeat_interleave(g, 0).to(case.q.dtype)
+    run = GpuRun(case, period=period).run(0, wl.steps)
+    compare_decode(run, wl.steps)
+    hist = run.focal_history
+    assert [t for t, _ in hist] == [wl.warmup - 1 + m * period for m in range(3)]
+    assert hist[0][1] == tuple(first)
+    assert not set(hist[1][1]) & set(first)
+
+
+@pytest.mark.parametrize("splits", [None, {0: 5, 1: 4, 2: 5}], ids=["auto", "forced"])
+def test_ragged_batch(splits):
+    """One launch over sequences that differ in cache length, image position,
+    image count (hence k) and R-SWA window position -- as in a continuously
+    batched server: every sequence matches the oracle run on its own. Forced
+    split counts also give some CTAs of the short sequences little or nothing
+    to stream."""
+    from dynamic_sparse_kv_gb300 import DecodeAttention
+    from dynamic_sparse_kv_gb300 import _native as N
+    case = _case("qwen7b_b1", batch=4, layers=1, prompt=40, grid=(1, 16, 20), steps=70, tau=0.07)
+    wl = case.wl
+    n_max = wl.seq_len_at(69)                       # 430
+    n_ts = [n_max, n_max - 17, wl.prompt + wl.n_img + 1, n_max - 35]
+    ranges = [(40, 320), (23, 300), (40, 250), (0, 320)]   # (start, N_img), inside [0, N_t)
+    prefix, window = 100, 24
+    dec = DecodeAttention(case.k_cache, case.v_cache, case.block_table, q_heads=wl.q_heads,
+                          img_range=case.img_range, max_img=wl.n_img, tau=wl.tau, splits=splits)
+    dec.set_seq_len(n_max)                          # length hint: the longest sequence
+    dec.set_seq_len(torch.tensor(n_ts, dtype=torch.int32, device="cuda"))
+    img = torch.tensor(ranges, dtype=torch.int32, device="cuda")
+    q = case.q_at(69)[0].contiguous()
+    out_full, out_focal, out_sparse, out_rswa = (torch.empty_like(q) for _ in range(4))
+    idx = torch.zeros(wl.batch, dec.stride, dtype=torch.int32, device="cuda")
+    k = torch.zeros(wl.batch, dtype=torch.int32, device="cuda")
+    N.fastocr_full_attend(dec.handle, q, dec.kv[0], out_full)
+    N.fastocr_focal_attend(dec.handle, q, dec.kv[0], img, wl.tau, out_focal, idx, dec.stride, k)
+    N.fastocr_sparse_attend(dec.handle, q, dec.kv[0], img, idx, dec.stride, k, out_sparse)
+    N.fastocr_rswa_attend(dec.handle, q, dec.kv[0], prefix, window, out_rswa)
+    torch.cuda.synchronize()
+    assert dec.device_status() == 0
+    kv = KVCache(case)
+    for b, (n_t, (start, n_img)) in enumerate(zip(n_ts, ranges)):
+        Kl, Vl = kv(0, b)
+        qb = np64(q[b])
+        assert_close(out_full[b], A.full_attend(qb, Kl, Vl, n_t), TOL["bf16"], f"full b={b}")
+        ref_out, ref_sel, sigma = A.focal_attend(qb, Kl, Vl, n_t, start, n_img, wl.tau)
+        assert_close(out_focal[b], ref_out, TOL["bf16"], f"focal b={b}")
+        kk = int(k[b])
+        assert kk == A.keep_count(wl.tau, n_img)
+        got = idx[b, :kk].cpu().numpy()
+        check_selection(got, ref_sel, sigma, start, f"focal b={b}")
+        assert_close(out_sparse[b], A.sparse_attend(qb, Kl, Vl, n_t, start, n_img, got),
+                     TOL["bf16"], f"sparse b={b}")
+        assert_close(out_rswa[b], A.rswa_attend(qb, Kl, Vl, n_t, prefix, window), TOL["bf16"],
+                     f"rswa b={b}")
+    dec.close()
+
+
 def test_sparse_selection_permutation_and_empty():
     """Gather order does not matter; an empty attend list gives zeros."""
     from dynamic_sparse_kv_gb300 import _native as N
