@@ -468,6 +468,28 @@ def run_gpu(args, rank, world, local_rank):
         torch.cuda.synchronize()
         compare["recapture_ms"] = (time.perf_counter() - c0) * 1e3
         del pcap
+        # latency floor of a decode step's launch chain: as many dependent
+        # one-element kernels as the step has layers, in one CUDA graph
+        tiny = torch.zeros(1, device=dev)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            tiny.add_(1.0)
+        torch.cuda.current_stream().wait_stream(side)
+        chain = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(chain):
+            for _ in range(wl.layers):
+                tiny.add_(1.0)
+        ts = []
+        for _ in range(W + 50):
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record()
+            chain.replay()
+            s1.record()
+            torch.cuda.synchronize()
+            ts.append(s0.elapsed_time(s1) * 1e3)
+        compare["launch_chain_floor_us_per_step"] = statistics.median(ts[W:])
+        del chain
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

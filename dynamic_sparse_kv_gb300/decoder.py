@@ -225,6 +225,12 @@ class DecodeAttention:
                                   self.rswa_window, out[l], stream)
 
     def launches_per_step(self, kind: str) -> int:
+        """Kernels one step of `kind` launches: one attend kernel per layer,
+        plus the selection kernel of every focal (or profiling) layer."""
+        if kind == "fastocr":
+            return self.layers + len(self.focal)
+        if kind == "profile":
+            return 2 * self.layers
         return self.layers
 
     def device_status(self, stream=None) -> int:
@@ -258,7 +264,7 @@ class CapturedStep:
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph):
             fn(self.q, self.out)
-        self.launches = dec.layers           # one kernel per layer call
+        self.launches = dec.launches_per_step(kind)
 
     def replay(self):
         self.graph.replay()

@@ -56,6 +56,11 @@
  *  former must be written before the kernel preceding the call starts -- in
  *  a decode step they are set once before the first layer -- while q, the
  *  selection and the current token may come from the kernel right before.
+ *  One exception: a gather (sparse) call stages the rows of the selection it
+ *  expects before that kernel completes, so if img_range contains the
+ *  current token N_t - 1 (the image normally ends before the generated
+ *  text), that token's K/V must be written before the preceding kernel
+ *  starts as well.
  *
  *  Errors: argument errors are detected on the host and returned as a
  *  negative status before anything is launched. Faults in device data (page

@@ -270,6 +270,52 @@ def test_ragged_batch(splits):
     dec.close()
 
 
+@pytest.mark.parametrize("splits", [None, {0: 16, 1: 16, 2: 16}], ids=["auto", "split16"])
+def test_degenerate_lengths(splits):
+    """Edge cases in one launch: a cache of only the current token, an image
+    range that is empty, starts at N_t, or holds the current token (which a
+    gather layer then attends only if it was selected), and -- with 16
+    splits -- CTAs that have nothing at all to stream."""
+    from dynamic_sparse_kv_gb300 import DecodeAttention
+    from dynamic_sparse_kv_gb300 import _native as N
+    case = _case("qwen7b_b1", batch=6, layers=1, prompt=16, grid=(1, 4, 8), steps=8, tau=0.5)
+    wl = case.wl
+    n_ts = [1, 2, 17, 1, 40, 3]
+    ranges = [(0, 0), (0, 2), (16, 0), (1, 0), (5, 30), (0, 3)]
+    prefix, window = 100, 24
+    dec = DecodeAttention(case.k_cache, case.v_cache, case.block_table, q_heads=wl.q_heads,
+                          img_range=case.img_range, max_img=wl.n_img, tau=wl.tau, splits=splits)
+    dec.set_seq_len(max(n_ts))
+    dec.set_seq_len(torch.tensor(n_ts, dtype=torch.int32, device="cuda"))
+    img = torch.tensor(ranges, dtype=torch.int32, device="cuda")
+    q = case.q_at(0)[0].contiguous()
+    out_full, out_focal, out_sparse, out_rswa = (torch.full_like(q, 7.0) for _ in range(4))
+    idx = torch.full((wl.batch, dec.stride), -5, dtype=torch.int32, device="cuda")
+    k = torch.full((wl.batch,), -5, dtype=torch.int32, device="cuda")
+    N.fastocr_full_attend(dec.handle, q, dec.kv[0], out_full)
+    N.fastocr_focal_attend(dec.handle, q, dec.kv[0], img, wl.tau, out_focal, idx, dec.stride, k)
+    N.fastocr_sparse_attend(dec.handle, q, dec.kv[0], img, idx, dec.stride, k, out_sparse)
+    N.fastocr_rswa_attend(dec.handle, q, dec.kv[0], prefix, window, out_rswa)
+    torch.cuda.synchronize()
+    assert dec.device_status() == 0
+    kv = KVCache(case)
+    for b, (n_t, (start, n_img)) in enumerate(zip(n_ts, ranges)):
+        Kl, Vl = kv(0, b)
+        qb = np64(q[b])
+        assert_close(out_full[b], A.full_attend(qb, Kl, Vl, n_t), TOL["bf16"], f"full b={b}")
+        ref_out, ref_sel, sigma = A.focal_attend(qb, Kl, Vl, n_t, start, n_img, wl.tau)
+        assert_close(out_focal[b], ref_out, TOL["bf16"], f"focal b={b}")
+        kk = int(k[b])
+        assert kk == A.keep_count(wl.tau, n_img) == len(ref_sel)
+        got = idx[b, :kk].cpu().numpy()
+        check_selection(got, ref_sel, sigma, start, f"focal b={b}")
+        assert_close(out_sparse[b], A.sparse_attend(qb, Kl, Vl, n_t, start, n_img, got),
+                     TOL["bf16"], f"sparse b={b}")
+        assert_close(out_rswa[b], A.rswa_attend(qb, Kl, Vl, n_t, prefix, window), TOL["bf16"],
+                     f"rswa b={b}")
+    dec.close()
+
+
 def test_sparse_selection_permutation_and_empty():
     """Gather order does not matter; an empty attend list gives zeros."""
     from dynamic_sparse_kv_gb300 import _native as N
