@@ -9,8 +9,12 @@ FastOCR (gist.science technical summary, "Focal-Guided Pruning" and
     head-summed image scores, top ceil(tau*N_img)); the selection is handed
     to the following non-focal layers (fastocr_sparse_attend);
   * non-focal layers before the first focal layer reuse F_last, the previous
-    step's selection of the deepest focal layer.
-Unlimited OCR (R-SWA): every layer calls fastocr_rswa_attend.
+    step's selection of the deepest focal layer;
+  * adaptive layer selection (named there as future work): ProfileSchedule
+    re-runs the warm-up window every `period` steps and re-chooses C.
+Unlimited OCR (R-SWA): every layer calls fastocr_rswa_attend; with
+ring_block_table a sequence's cache holds only the prefix and a ring of
+window pages.
 
 The selection never leaves the GPU: every focal layer writes into its own
 fixed device buffer, and F_last *is* the deepest focal layer's buffer, which
