@@ -344,10 +344,13 @@ __device__ __forceinline__ void add_selection(const Params& p, int k, int split,
 // ST: cp.async pipeline depth per warp (kStages, or kStagesDeep for grids
 // small enough that every CTA has an SM of its own).
 template <typename T, int D, int MODE, int ST>
-__global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
+__global__ void __launch_bounds__(32 * warps_for(ST), 2) attend_kernel(const Params p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   using SM = Smem<T, D, ST>;
-  using E = EpiSmem<D>;
+  constexpr int kWarps = warps_for(ST);
+  constexpr int kThreads = 32 * kWarps;
+  constexpr int kSliceMax = slice_for(ST);
+  using E = EpiSmem<D, kWarps>;
   constexpr bool kMma = sizeof(T) == 2;
   constexpr int ROWB = SM::kRowBytes;
   constexpr int CH = ROWB / 16;                 // 16-byte chunks per row
@@ -1114,7 +1117,7 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(const Params p) {
 template <typename T, int D, int MODE, int ST>
 cudaError_t launch_attend(const Params& p, cudaStream_t stream) {
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = pdl_config(dim3(p.splits, p.Hkv, p.B), dim3(kThreads, 1, 1),
+  cudaLaunchConfig_t cfg = pdl_config(dim3(p.splits, p.Hkv, p.B), dim3(32 * warps_for(ST), 1, 1),
                                       attend_smem_bytes<T, D, ST>(), stream, attr);
   attr[1].id = cudaLaunchAttributeClusterDimension;   // the splits of one (b, hkv)
   attr[1].val.clusterDim.x = p.splits;
@@ -1175,7 +1178,7 @@ template <typename T, int D>
 int active_clusters(int c) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(c, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(32 * warps_for(kStages), 1, 1);
   cfg.dynamicSmemBytes = attend_smem_bytes<T, D>();
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1200,7 +1203,7 @@ int max_cluster_size() {
   for (int c = kMaxSplits; c > 1; c >>= 1) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(c, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(32 * warps_for(ST), 1, 1);
     cfg.dynamicSmemBytes = attend_smem_bytes<T, D, ST>();
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

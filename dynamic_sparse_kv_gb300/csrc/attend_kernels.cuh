@@ -11,11 +11,11 @@
 //
 // Work decomposition (split-K flash-decode): grid = (splits, H_kv, B); the S
 // splits of one (sequence, KV head) form a thread-block cluster. A CTA owns a
-// contiguous slice of that KV head's attend list; its four warps stream
-// 16-token tiles of the slice independently through a cp.async pipeline (3
-// stages; 6 for grids that leave every CTA an SM of its own), in 16-byte
-// chunks into XOR-swizzled rows, so any gathered row is a coalesced 256-byte
-// read and ldmatrix is conflict-free. For bf16 the GQA group (g <= 8 query
+// contiguous slice of that KV head's attend list; its warps stream 16-token
+// tiles of the slice independently through a cp.async pipeline (6 warps of 2
+// stages; 4 warps of 6 stages for grids that leave every CTA an SM of its
+// own), in 16-byte chunks into XOR-swizzled rows, so any gathered row is a
+// coalesced 256-byte read and ldmatrix is conflict-free. For bf16 the GQA group (g <= 8 query
 // heads) x 16 keys contraction and the P.V product run on the tensor cores
 // (mma.sync m16n8k16, keys / head dims on M, query heads on N); fp32 runs on
 // the CUDA cores. Softmax is online in the base-2 domain with a lazily moved
@@ -34,12 +34,16 @@
 
 namespace fastocr {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 16;      // tokens per warp tile
 constexpr int kSlots = 8;      // query-head slots per KV head (g <= 8)
-constexpr int kStages = 3;     // cp.async pipeline depth per warp (two CTAs per SM)
+constexpr int kStages = 2;     // cp.async pipeline depth per warp (two CTAs per SM)
 constexpr int kStagesDeep = 6; // depth of the variant for grids that leave an SM per CTA
+// Warps per CTA of each variant. The general one runs 6 warps of 2 stages:
+// with one CTA of a grid on an SM, a warp's tile loop is bound by its own
+// instruction latency, so more warps stream faster, and 12 stages still let
+// two CTAs share an SM. The deep one keeps 4 warps of 6 stages, so a
+// batch-1 CTA stages its whole share before the wait.
+__host__ __device__ constexpr int warps_for(int st) { return st == kStagesDeep ? 4 : 6; }
 constexpr float kLazyMax = 8.f; // running-max slack (log2 units) before a rescale
 constexpr int kMaxSplits = 16;  // = the largest thread-block cluster used
 constexpr int kMaxImg = 16384; // image tokens whose scores fit in shared memory
@@ -237,10 +241,15 @@ __device__ __forceinline__ AttendList make_list(const Params& p, int b, int& bad
 
 // ---------------------------------------------------------------- shared memory
 
-constexpr int kSliceMax = 1024;  // work-list entries resolved to cache rows per round
+// Work-list entries resolved to cache rows per round: a multiple of the CTA
+// size (every thread resolves the same number).
+__host__ __device__ constexpr int slice_for(int st) { return warps_for(st) == 4 ? 1024 : 960; }
 
 template <typename T, int D, int ST = kStages>
 struct Smem {
+  static constexpr int kWarps = warps_for(ST);
+  static constexpr int kSliceMax = slice_for(ST);
+  static_assert(kSliceMax % (32 * kWarps) == 0 && kSliceMax % kTile == 0, "slice layout");
   static constexpr int kRowBytes = D * (int)sizeof(T);
   static constexpr int kStageBytes = 2 * kTile * kRowBytes;          // K rows then V rows
   static constexpr int kPipeBytes = kWarps * ST * kStageBytes;
@@ -257,7 +266,7 @@ struct Smem {
   static constexpr int kMainBytes = kQOffset + (sizeof(T) == 4 ? kSlots * D * 4 : 0);
 };
 
-template <int D>
+template <int D, int kWarps>
 struct EpiSmem {
   // reuses the pipeline area once streaming is done: per-warp partials
   // wm[W][8], wl[W][8], wacc[W][8][D]; focal: the heads' max M[8], 1/sum invL[8]
@@ -271,7 +280,8 @@ struct EpiSmem {
 
 template <typename T, int D, int ST = kStages>
 inline int attend_smem_bytes() {
-  static_assert(EpiSmem<D>::kBytes <= Smem<T, D, ST>::kPipeBytes, "epilogue must fit the pipeline area");
+  static_assert(EpiSmem<D, warps_for(ST)>::kBytes <= Smem<T, D, ST>::kPipeBytes,
+                "epilogue must fit the pipeline area");
   return Smem<T, D, ST>::kMainBytes;
 }
 
