@@ -8,7 +8,20 @@ full attention + image scores + top-k; other layers: gather attention over
 prompt + selected image tokens + generated tokens, with Cross-Step Fixation
 Reuse), captured once in a CUDA graph and replayed. Inputs are synthetic and
 seeded (synth module) and resident in HBM. L2 is flushed (512 MB memset,
-untimed) before every timed step. Prints one JSON line.
+untimed) before every timed step. The K-step timed pass is repeated until the
+timed work spans a few seconds (so the clock sampler sees it); the reported
+value is the median pass. Prints one JSON line.
+
+The headline workload is `serving_b32` (32 sequences x 8192 image tokens, the
+largest single-GPU configuration); the batch-1 `qwen7b_b1` workload is
+measured in the same run and reported in the line's `secondary` block.
+
+Inside the line, `config.kernels` gives each layer kind's share of the step:
+the step's layers of one kind (focal: attend + selection; sparse: gather
+attend) captured alone in a graph, in step order, and replayed like the step,
+so the kinds' times add up to about the step (`kinds_sum_over_step`); the
+roofline record takes the kind with the largest share. `alone` gives one
+launch of each kind timed by itself (its own graph, L2 flushed).
 
 --impl reference times the CPU oracle (fp64 NumPy, one thread) on a bounded
 sample of the same workload instead -- the deliberately slow baseline.
@@ -21,6 +34,7 @@ import argparse
 import dataclasses
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -34,16 +48,23 @@ if ROOT not in sys.path:
 METRIC = "decode attention steps/s and µs/step at tau=0.05; achieved HBM GB/s vs peak"
 FALLBACK_HBM_GBS = 6800.0
 FLUSH_BYTES = 512 << 20
+PROBE_BYTES = 2 << 30
 CSRC = os.path.join(ROOT, "dynamic_sparse_kv_gb300", "csrc")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.md")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_NAME = {"focal": "attend_focal", "sparse": "attend_sparse", "rswa": "attend_rswa",
+               "full": "attend_full"}
 
 
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="qwen7b_b1")
+    ap.add_argument("--workload", default="serving_b32")
+    ap.add_argument("--secondary", default="qwen7b_b1",
+                    help="second workload reported in the same line ('none' to skip)")
+    ap.add_argument("--soak", type=float, default=4.0,
+                    help="seconds of timed passes (repeats of the K-step pass)")
     ap.add_argument("--tau", type=float, default=None)
     ap.add_argument("--set", action="append", default=[], metavar="FIELD=VALUE",
                     help="override a workload field, e.g. --set batch=8 (profiling runs)")
@@ -51,6 +72,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-compare", action="store_true", help="skip the dense / tau=1 arms")
+    ap.add_argument("--no-probe", action="store_true", help="skip the read-only bandwidth probe")
     ap.add_argument("--rswa-ring", action="store_true",
                     help="R-SWA: keep only prefix + window pages per sequence (ring block table)")
     ap.add_argument("--oracle-leg", default=None, help=argparse.SUPPRESS)
@@ -102,18 +124,23 @@ def source_digest() -> str:
 
 
 def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources (line: `traffic <kernel> <workload> <bytes> <digest>`)."""
+    """DRAM bytes per launch from a committed ncu summary (profiles/traffic.json),
+    if it was taken on the current kernel sources."""
     try:
         with open(TRAFFIC_FILE) as f:
-            for line in f:
-                parts = line.strip().strip("`").split()
-                if len(parts) == 5 and parts[0] == "traffic" and parts[1] == kernel \
-                        and parts[2] == workload:
-                    return float(parts[3]) if parts[4] == source_digest() else None
-    except OSError:
-        pass
+            entries = json.load(f)["entries"]
+    except (OSError, ValueError, KeyError):
+        return None
+    for e in entries:
+        if e.get("kernel") == kernel and e.get("workload") == workload:
+            return float(e["bytes_per_launch"]) if e.get("digest") == source_digest() else None
     return None
+
+
+def median_index(xs):
+    """Index of the median element (lower median)."""
+    order = sorted(range(len(xs)), key=lambda i: xs[i])
+    return order[(len(xs) - 1) // 2]
 
 
 class ClockSampler:
@@ -128,7 +155,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "20", "-i", gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                 "-lms", "50", "-i", gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
                 text=True)
         except OSError:
             self.proc = None
@@ -257,52 +284,87 @@ def kv_bytes(wl, kind: str, n_t: int, k_per_seq) -> float:
     return float(tot)
 
 
-def run_gpu(args, rank, world, local_rank):
+def kinds_check(kernels: dict, us_per_step: float) -> dict:
+    """How the per-kind in-step times add up against the step."""
+    tot = sum(v["us_in_step"] for v in kernels.values())
+    return {"kinds_sum_us": tot, "kinds_sum_over_step": tot / us_per_step,
+            "kinds_exceed_step": tot > 1.10 * us_per_step}
+
+
+def read_probe(dev, flush, world):
+    """Read-only HBM bandwidth: fastocr_read_probe over 2 GiB (16x L2), L2
+    flushed before each of 12 timed reads; median and best GB/s."""
     import torch
 
-    import synth
-    from dynamic_sparse_kv_gb300 import CapturedStep, DecodeAttention
     import dynamic_sparse_kv_gb300._native as N
+    buf = torch.ones(PROBE_BYTES, dtype=torch.uint8, device=dev)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    times = []
+    for r in range(15):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        N.fastocr_read_probe(buf, PROBE_BYTES, sink)
+        e.record()
+        torch.cuda.synchronize()
+        if r >= 3:
+            times.append(s.elapsed_time(e) * 1e-3)
+    del buf
+    torch.cuda.empty_cache()
+    med = reduce_max(statistics.median(times), world, dev)
+    return {"gbs": PROBE_BYTES / med / 1e9, "best_gbs": PROBE_BYTES / min(times) / 1e9,
+            "bytes": PROBE_BYTES, "reads": len(times),
+            "how": "fastocr_read_probe: one read of every 16-byte word, ld.global.nc, "
+                   "L2 flushed before each read, CUDA events, median"}
 
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    wl = synth.workload(args.workload)
-    if args.tau is not None:
-        wl = wl.with_(tau=args.tau)
-    for item in args.set:
-        key, val = item.split("=", 1)
-        wl = wl.with_(**{key: type(getattr(wl, key))(val)})
-    wl = wl.with_(seed=wl.seed + 1000 * rank)
-    K, W = args.steps, args.warmup
-    assert W >= 3, "at least 3 warm-up steps"
-    if wl.mode == "fastocr":
-        t0_steady, step0 = wl.warmup, 0         # the warm-up reads steps [0, warmup)
-    else:   # R-SWA: the last steps before T = wl.steps generated tokens (window full)
-        t0_steady = step0 = max(0, wl.steps - (W + K))
-    span = wl.steps - t0_steady                 # steady steps available in the workload
-    n_gen = min(wl.steps, t0_steady + W + K) - step0
-    case = synth.make_case(wl, device=dev, step0=step0, n_steps=n_gen)
-    storage = "full"
-    if wl.mode == "rswa" and args.rswa_ring:
-        # bounded memory: pages past the prefix form a ring of ceil(n / page)
-        # pages per sequence; the timed kernels are the same
-        from dynamic_sparse_kv_gb300 import ring_block_table
-        table, per = ring_block_table(wl.batch, wl.rswa_prefix, wl.rswa_window, wl.page_size,
-                                      wl.max_tokens)
-        n_pages = wl.batch * per
-        k_ring = case.k_cache[:, :n_pages].clone()
-        v_ring = case.v_cache[:, :n_pages].clone()
-        case = dataclasses.replace(case, k_cache=k_ring, v_cache=v_ring,
-                                   block_table=table.to(dev))
-        torch.cuda.empty_cache()
-        storage = "ring"
 
-    def t_of(i):                                # i-th bench step -> decode step index
-        return t0_steady + (i % min(span, n_gen - (t0_steady - step0)))
+class Bench:
+    """One workload on one GPU: case, decoder, graphs and their timings."""
 
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    def __init__(self, args, name, rank, world, dev, flush, tau=None, overrides=()):
+        import torch
 
-    def build(tau, kind):
+        import synth
+        self.torch = torch
+        self.args, self.rank, self.world, self.dev, self.flush = args, rank, world, dev, flush
+        wl = synth.workload(name)
+        if tau is not None:
+            wl = wl.with_(tau=tau)
+        for item in overrides:
+            key, val = item.split("=", 1)
+            wl = wl.with_(**{key: type(getattr(wl, key))(val)})
+        self.wl = wl = wl.with_(seed=wl.seed + 1000 * rank)
+        K, W = args.steps, args.warmup
+        if wl.mode == "fastocr":
+            self.t0_steady, step0 = wl.warmup, 0        # the warm-up reads steps [0, warmup)
+        else:   # R-SWA: the last steps before T = wl.steps generated tokens (window full)
+            self.t0_steady = step0 = max(0, wl.steps - (W + K))
+        self.span = wl.steps - self.t0_steady        # steady steps available in the workload
+        self.n_gen = min(wl.steps, self.t0_steady + W + K) - step0
+        case = synth.make_case(wl, device=dev, step0=step0, n_steps=self.n_gen)
+        self.storage = "full"
+        if wl.mode == "rswa" and args.rswa_ring:
+            # bounded memory: pages past the prefix form a ring of ceil(n / page)
+            # pages per sequence; the timed kernels are the same
+            from dynamic_sparse_kv_gb300 import ring_block_table
+            table, per = ring_block_table(wl.batch, wl.rswa_prefix, wl.rswa_window, wl.page_size,
+                                          wl.max_tokens)
+            n_pages = wl.batch * per
+            k_ring = case.k_cache[:, :n_pages].clone()
+            v_ring = case.v_cache[:, :n_pages].clone()
+            case = dataclasses.replace(case, k_cache=k_ring, v_cache=v_ring,
+                                       block_table=table.to(dev))
+            torch.cuda.empty_cache()
+            self.storage = "ring"
+        self.case = case
+        self.kind = "rswa" if wl.mode == "rswa" else "fastocr"
+
+    def t_of(self, i):                       # i-th bench step -> decode step index
+        return self.t0_steady + (i % min(self.span, self.n_gen - (self.t0_steady - self.case.step0)))
+
+    def build(self, tau, kind):
+        from dynamic_sparse_kv_gb300 import CapturedStep, DecodeAttention
+        wl, case = self.wl, self.case
         dec = DecodeAttention(case.k_cache, case.v_cache, case.block_table, q_heads=wl.q_heads,
                               img_range=case.img_range, max_img=wl.n_img, tau=tau, mode=wl.mode,
                               rswa_prefix=wl.rswa_prefix, rswa_window=wl.rswa_window)
@@ -312,124 +374,169 @@ def run_gpu(args, rank, world, local_rank):
                 dec.set_focal_layers(wl.focal_layers)
                 focal = tuple(wl.focal_layers)
             else:
-                qw = torch.empty_like(case.q_at(0))
+                qw = self.torch.empty_like(case.q_at(0))
                 dec.begin_warmup()
                 for t in range(wl.warmup):   # the method's profiling warm-up (untimed)
                     dec.set_seq_len(wl.seq_len_at(t))
                     dec.warmup_step(case.q_at(t).contiguous(), qw)
                 focal, _ = dec.finish_warmup(wl.n_focal)
-        dec.set_seq_len(wl.seq_len_at(t_of(0)))
+        dec.set_seq_len(self.wl.seq_len_at(self.t_of(0)))
         return dec, focal, CapturedStep(dec, kind)
 
-    def stage(dec, cap, i):
-        t = t_of(i)
-        dec.set_seq_len(wl.seq_len_at(t))
-        cap.q.copy_(case.q_at(t))
+    def stage(self, dec, cap, i):
+        t = self.t_of(i)
+        dec.set_seq_len(self.wl.seq_len_at(t))
+        cap.q.copy_(self.case.q_at(t))
 
-    def time_graph(dec, cap, n_warm, n_timed, sampler_gpu=None):
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_timed)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_timed)]
-        for i in range(n_warm):
-            stage(dec, cap, i)
-            flush.zero_()
+    def time_graph(self, dec, cap, soak_s, sampler_gpu=None, min_passes=3, max_passes=2000):
+        """Warm-up W steps, then repeat the K-step timed pass (L2 flushed before
+        every step, untimed) for about soak_s seconds. Returns (median pass ms
+        summed over its K steps, all pass totals, wall seconds, clocks)."""
+        torch = self.torch
+        K, W = self.args.steps, self.args.warmup
+        for i in range(W):
+            self.stage(dec, cap, i)
+            self.flush.zero_()
             cap.replay()
         torch.cuda.synchronize()
-        barrier(world)
+        barrier(self.world)
+
+        def one_pass(i0):
+            starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+            ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+            for j in range(K):
+                self.stage(dec, cap, i0 + j)
+                self.flush.zero_()
+                starts[j].record()
+                cap.replay()
+                ends[j].record()
+            torch.cuda.synchronize()
+            return sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+
         sampler = ClockSampler(sampler_gpu) if sampler_gpu else None
         wall0 = time.perf_counter()
-        for j in range(n_timed):
-            stage(dec, cap, n_warm + j)
-            flush.zero_()
-            starts[j].record()
-            cap.replay()
-            ends[j].record()
-        torch.cuda.synchronize()
+        passes = [one_pass(W)]
+        first = time.perf_counter() - wall0
+        n = int(min(max_passes, max(min_passes, math.ceil(soak_s / max(first, 1e-6)))))
+        n = int(reduce_max(float(n), self.world, self.dev))   # same pass count on every rank
+        for p in range(1, n):
+            passes.append(one_pass(W + p * K))
         wall = time.perf_counter() - wall0
         clocks = sampler.stop() if sampler else None
-        barrier(world)
-        per = [s.elapsed_time(e) for s, e in zip(starts, ends)]      # ms
-        return per, wall, clocks
+        barrier(self.world)
+        med = statistics.median(passes)
+        return reduce_max(med, self.world, self.dev), passes, wall, clocks
 
-    gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
-    kind = "rswa" if wl.mode == "rswa" else "fastocr"
-    dec, focal, cap = build(wl.tau, kind)
-    per, wall, clocks = time_graph(dec, cap, W, K, sampler_gpu=gpu_uuid)
-    total_ms = reduce_max(sum(per), world, dev)
-    status = dec.device_status()
-    assert status == 0, f"device status {status}"
+    def time_replays(self, dec, cap, n):
+        """Median µs of n replays of cap (steps staged as in the timed pass, L2
+        flushed before each), and the staged decode steps."""
+        torch = self.torch
+        W = self.args.warmup
+        ts, steps = [], []
+        for i in range(W + n):
+            self.stage(dec, cap, i)
+            self.flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            cap.replay()
+            e.record()
+            torch.cuda.synchronize()
+            if i >= W:
+                ts.append(s.elapsed_time(e) * 1e3)
+                steps.append(self.t_of(i))
+        return reduce_max(statistics.median(ts), self.world, self.dev), steps
 
-    # ---- per-kernel durations (eager launches queued behind a sleep, events between)
-    def layer_kind(l):
+    # ---- per-kind graphs: the step's layers of one kind, in step order
+    def kind_fns(self, dec):
+        import dynamic_sparse_kv_gb300._native as N
+        wl = self.wl
+        if self.kind == "rswa":
+            def rswa(q, out, stream=None):
+                dec.rswa_step(q, out, stream)
+            return {"rswa": (rswa, dec.layers, dec.layers)}
+        focal = set(dec.sel)
+
+        def only(kind):
+            def fn(q, out, stream=None):
+                cur = dec.sel[max(dec.focal)]
+                for l in range(dec.layers):
+                    if l in focal:
+                        idx, k = dec.sel[l]
+                        if kind == "focal":
+                            N.fastocr_focal_attend(dec.handle, q[l], dec.kv[l], dec.img_range,
+                                                   dec.tau, out[l], idx, dec.stride, k, -1,
+                                                   stream)
+                        cur = (idx, k)
+                    elif kind == "sparse":
+                        N.fastocr_sparse_attend(dec.handle, q[l], dec.kv[l], dec.img_range,
+                                                cur[0], dec.stride, cur[1], out[l], stream)
+            return fn
+        n_f = len(focal)
+        return {"focal": (only("focal"), n_f, 2 * n_f),
+                "sparse": (only("sparse"), wl.layers - n_f, wl.layers - n_f)}
+
+    def single_fn(self, dec, kind):
+        """One launch of `kind` (its first layer in the step)."""
+        import dynamic_sparse_kv_gb300._native as N
         if kind == "rswa":
-            return "rswa"
-        return "focal" if l in dec.sel else "sparse"
+            def fn(q, out, stream=None):
+                N.fastocr_rswa_attend(dec.handle, q[0], dec.kv[0], self.wl.rswa_prefix,
+                                      self.wl.rswa_window, out[0], stream)
+            return fn
+        first_focal = min(dec.sel)
+        first_sparse = next(l for l in range(dec.layers) if l not in dec.sel)
 
-    n_kt = min(K, 50)
-    kt = {"focal": [], "sparse": [], "rswa": [], "full": []}
-    kbytes = {"focal": [], "sparse": [], "rswa": [], "full": []}
-    stream = torch.cuda.current_stream()
-    for j in range(n_kt):
-        stage(dec, cap, W + j)
-        flush.zero_()
-        torch.cuda._sleep(4_000_000)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(dec.layers + 1)]
-        ev[0].record()
-        cur = dec.sel[max(dec.focal)] if kind == "fastocr" else None
-        for l in range(dec.layers):
-            if kind == "rswa":
-                N.fastocr_rswa_attend(dec.handle, cap.q[l], dec.kv[l], wl.rswa_prefix,
-                                      wl.rswa_window, cap.out[l], stream)
-            elif l in dec.sel:
-                idx, kk = dec.sel[l]
-                N.fastocr_focal_attend(dec.handle, cap.q[l], dec.kv[l], dec.img_range, dec.tau,
-                                       cap.out[l], idx, dec.stride, kk, -1, stream)
-                cur = (idx, kk)
+        def fn(q, out, stream=None):
+            src = dec.sel[max(dec.focal)]
+            if kind == "focal":
+                idx, k = dec.sel[first_focal]
+                N.fastocr_focal_attend(dec.handle, q[first_focal], dec.kv[first_focal],
+                                       dec.img_range, dec.tau, out[first_focal], idx, dec.stride,
+                                       k, -1, stream)
             else:
-                N.fastocr_sparse_attend(dec.handle, cap.q[l], dec.kv[l], dec.img_range, cur[0],
-                                        dec.stride, cur[1], cap.out[l], stream)
-            ev[l + 1].record()
-        torch.cuda.synchronize()
-        n_t = wl.seq_len_at(t_of(W + j))
-        k_seq = dec.sel[max(dec.focal)][1].tolist() if kind == "fastocr" else None
-        for l in range(dec.layers):
-            kd = layer_kind(l)
-            kt[kd].append(ev[l].elapsed_time(ev[l + 1]) * 1e-3)      # s
-            kbytes[kd].append(kv_bytes(wl, kd, n_t, k_seq))
-    peak, peak_src = measured_peaks()
-    kernels = {}
-    for kd in kt:
-        if not kt[kd]:
-            continue
-        launches_per_step = len(kt[kd]) / n_kt
-        mean_s = statistics.fmean(kt[kd])
-        bpl = statistics.fmean(kbytes[kd])
-        kernels[kd] = {"launches_per_step": launches_per_step, "us_per_launch": mean_s * 1e6,
-                       "kv_bytes_per_launch": bpl, "gbs": bpl / mean_s / 1e9,
-                       "share": launches_per_step * mean_s}
-    tot_share = sum(v["share"] for v in kernels.values())
-    for v in kernels.values():
-        v["share"] = v["share"] / tot_share
-    dom = max(kernels, key=lambda k: kernels[k]["share"])
-    kname = {"focal": "attend_focal", "sparse": "attend_sparse", "rswa": "attend_rswa",
-             "full": "attend_full"}[dom]
-    roofline = {"bound": "hbm", "kernel": kname, "achieved": kernels[dom]["gbs"], "peak": peak,
-                "unit": "GB/s", "frac": kernels[dom]["gbs"] / peak,
-                "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
-                if peak_src == "measured" else "fallback 6.8 TB/s",
-                "traffic": recorded_traffic(kname, wl.name)}
+                N.fastocr_sparse_attend(dec.handle, q[first_sparse], dec.kv[first_sparse],
+                                        dec.img_range, src[0], dec.stride, src[1],
+                                        out[first_sparse], stream)
+        return fn
 
-    # ---- end to end through the public API with host buffers
-    e2e = None
-    if not args.no_e2e:
-        q_host = torch.empty((n_gen,) + tuple(cap.q.shape), dtype=cap.q.dtype, pin_memory=True)
+    def kernel_breakdown(self, dec, us_per_step, n_rep):
+        from dynamic_sparse_kv_gb300 import CapturedStep
+        wl = self.wl
+        kernels, alone = {}, {}
+        for kind, (fn, layers, launches) in self.kind_fns(dec).items():
+            cap = CapturedStep(dec, kind, fn=fn, launches=launches)
+            us, steps = self.time_replays(dec, cap, n_rep)
+            del cap
+            k_seq = dec.sel[max(dec.focal)][1].tolist() if self.kind == "fastocr" else None
+            bpl = statistics.fmean(kv_bytes(wl, kind, wl.seq_len_at(t), k_seq) for t in steps)
+            kernels[kind] = {"layers_per_step": layers, "launches_per_step": launches,
+                             "us_in_step": us, "us_per_layer": us / layers,
+                             "kv_bytes_per_layer": bpl, "gbs": bpl * layers / (us * 1e-6) / 1e9,
+                             "share": us / us_per_step}
+            cap1 = CapturedStep(dec, kind + "_alone", fn=self.single_fn(dec, kind),
+                                launches=launches // layers)
+            us1, steps1 = self.time_replays(dec, cap1, n_rep)
+            del cap1
+            b1 = statistics.fmean(kv_bytes(wl, kind, wl.seq_len_at(t), k_seq) for t in steps1)
+            alone[kind] = {"us": us1, "kv_bytes": b1, "gbs": b1 / (us1 * 1e-6) / 1e9}
+        return kernels, alone
+
+    def e2e(self, dec, cap):
+        """Same step through the public API with the inputs copied from pinned
+        host memory and the outputs read back every step, inside the timing."""
+        torch = self.torch
+        K, W = self.args.steps, self.args.warmup
+        case, wl = self.case, self.wl
+        q_host = torch.empty((self.n_gen,) + tuple(cap.q.shape), dtype=cap.q.dtype,
+                             pin_memory=True)
         q_host.copy_(case.q)
         out_host = torch.empty(tuple(cap.out.shape), dtype=cap.out.dtype, pin_memory=True)
-        n_e = min(K, 200)
+        n_e = max(K, 50)
         s_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_e)]
         e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_e)]
         for j in range(W + n_e):
-            t = t_of(j)
-            flush.zero_()
+            t = self.t_of(j)
+            self.flush.zero_()
             if j >= W:
                 s_ev[j - W].record()
             dec.set_seq_len(wl.seq_len_at(t))
@@ -439,38 +546,19 @@ def run_gpu(args, rank, world, local_rank):
             if j >= W:
                 e_ev[j - W].record()
         torch.cuda.synchronize()
-        e_ms = reduce_max(sum(s.elapsed_time(e) for s, e in zip(s_ev, e_ev)), world, dev)
+        e_ms = reduce_max(sum(s.elapsed_time(e) for s, e in zip(s_ev, e_ev)), self.world,
+                          self.dev)
         qb = cap.q.numel() * cap.q.element_size() + 4 * wl.batch
-        e2e = {"value": world * n_e / (e_ms * 1e-3), "unit": "steps/s",
-               "h2d_bytes_per_step": qb, "d2h_bytes_per_step": cap.out.numel() * cap.out.element_size(),
-               "us_per_step": e_ms * 1e3 / n_e}
+        return {"value": self.world * n_e / (e_ms * 1e-3), "unit": "steps/s",
+                "h2d_bytes_per_step": qb,
+                "d2h_bytes_per_step": cap.out.numel() * cap.out.element_size(),
+                "us_per_step": e_ms * 1e3 / n_e, "steps": n_e}
 
-    # ---- comparison arms: dense (every layer full) and the tau = 1 FastOCR pipeline
-    compare = {}
-    if not args.no_compare and kind == "fastocr":
-        dcap = CapturedStep(dec, "dense")
-        per_d, _, _ = time_graph(dec, dcap, W, min(K, 200))
-        compare["dense_us_per_step"] = statistics.fmean(per_d) * 1e3
-        dec1, _, cap1 = build(1.0, "fastocr")
-        per_1, _, _ = time_graph(dec1, cap1, W, min(K, 200))
-        compare["tau1_us_per_step"] = statistics.fmean(per_1) * 1e3
-        dec1.close()
-        # adaptive layer selection: the cost of one profiling step (full
-        # attention, scoring, selection and profile accumulation in every
-        # layer) and of capturing the steady step anew after C changes
-        pcap = CapturedStep(dec, "profile")
-        per_p, _, _ = time_graph(dec, pcap, W, min(K, 200))
-        compare["profile_us_per_step"] = statistics.fmean(per_p) * 1e3
-        torch.cuda.synchronize()
-        c0 = time.perf_counter()
-        del pcap
-        pcap = CapturedStep(dec, "fastocr")
-        torch.cuda.synchronize()
-        compare["recapture_ms"] = (time.perf_counter() - c0) * 1e3
-        del pcap
-        # latency floor of a decode step's launch chain: as many dependent
-        # one-element kernels as the step has layers, in one CUDA graph
-        tiny = torch.zeros(1, device=dev)
+    def launch_chain_floor(self):
+        """A CUDA graph of as many dependent one-element kernels as the step
+        has layers: the latency floor of a dependent launch chain."""
+        torch = self.torch
+        tiny = torch.zeros(1, device=self.dev)
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
@@ -478,18 +566,139 @@ def run_gpu(args, rank, world, local_rank):
         torch.cuda.current_stream().wait_stream(side)
         chain = torch.cuda.CUDAGraph()
         with torch.cuda.graph(chain):
-            for _ in range(wl.layers):
+            for _ in range(self.wl.layers):
                 tiny.add_(1.0)
         ts = []
-        for _ in range(W + 50):
+        for _ in range(self.args.warmup + 50):
             s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s0.record()
             chain.replay()
             s1.record()
             torch.cuda.synchronize()
             ts.append(s0.elapsed_time(s1) * 1e3)
-        compare["launch_chain_floor_us_per_step"] = statistics.median(ts[W:])
-        del chain
+        return statistics.median(ts[self.args.warmup:])
+
+    def compare_arms(self, dec):
+        """Dense (every layer full) and the tau = 1 FastOCR pipeline, timed like
+        the step; a profiling step and the re-capture cost of adaptive layer
+        selection."""
+        from dynamic_sparse_kv_gb300 import CapturedStep
+        torch = self.torch
+        compare = {}
+        dcap = CapturedStep(dec, "dense")
+        ms, _, _, _ = self.time_graph(dec, dcap, 1.0)
+        compare["dense_us_per_step"] = ms * 1e3 / self.args.steps
+        del dcap
+        dec1, _, cap1 = self.build(1.0, "fastocr")
+        ms, _, _, _ = self.time_graph(dec1, cap1, 1.0)
+        compare["tau1_us_per_step"] = ms * 1e3 / self.args.steps
+        del cap1
+        dec1.close()
+        pcap = CapturedStep(dec, "profile")
+        ms, _, _, _ = self.time_graph(dec, pcap, 0.5)
+        compare["profile_us_per_step"] = ms * 1e3 / self.args.steps
+        torch.cuda.synchronize()
+        c0 = time.perf_counter()
+        del pcap
+        pcap = CapturedStep(dec, "fastocr")
+        torch.cuda.synchronize()
+        compare["recapture_ms"] = (time.perf_counter() - c0) * 1e3
+        del pcap
+        return compare
+
+
+def run_workload(args, name, rank, world, dev, flush, *, headline, sampler_gpu=None):
+    """Measure one workload; returns (result dict, Bench, peak info)."""
+    torch = __import__("torch")
+    K = args.steps
+    bn = Bench(args, name, rank, world, dev, flush, tau=args.tau if headline else None,
+               overrides=args.set if headline else ())
+    wl = bn.wl
+    dec, focal, cap = bn.build(wl.tau, bn.kind)
+    ms_pass, passes, wall, clocks = bn.time_graph(dec, cap, args.soak if headline else 1.0,
+                                                  sampler_gpu=sampler_gpu)
+    status = dec.device_status()
+    assert status == 0, f"device status {status}"
+    us_per_step = ms_pass * 1e3 / K
+    n_rep = 30
+    kernels, alone = bn.kernel_breakdown(dec, us_per_step, n_rep)
+    check = kinds_check(kernels, us_per_step)
+    e2e = None if args.no_e2e else bn.e2e(dec, cap)
+    compare = {}
+    if not args.no_compare and bn.kind == "fastocr":
+        compare = bn.compare_arms(dec)
+    compare["launch_chain_floor_us_per_step"] = bn.launch_chain_floor()
+    step_bytes = sum(v["kv_bytes_per_layer"] * v["layers_per_step"] for v in kernels.values())
+    res = {
+        "workload": wl.name, "us_per_step": us_per_step, "steps_per_s": world * 1e6 / us_per_step,
+        "tau": wl.tau, "batch_per_gpu": wl.batch, "focal_layers": list(focal) if focal else None,
+        "kv_bytes_per_step": step_bytes,
+        "achieved_step_gbs": step_bytes / (us_per_step * 1e-6) / 1e9,
+        "timed_passes": len(passes), "pass_ms_min_median_max": [min(passes), ms_pass, max(passes)],
+        "wall_s_timed_passes": wall, "kernels": kernels, **check, "alone": alone,
+        "gpu_launches_per_step": cap.launches, **compare, "e2e": e2e,
+    }
+    if "dense_us_per_step" in compare:
+        res["speedup_vs_dense"] = compare["dense_us_per_step"] / us_per_step
+        res["speedup_vs_tau1"] = compare["tau1_us_per_step"] / us_per_step
+    if wl.mode == "rswa":
+        res.update({
+            "rswa_prefix": wl.rswa_prefix, "rswa_window": wl.rswa_window,
+            "generated_tokens_timed": [bn.t_of(args.warmup) + 1,
+                                       bn.t_of(args.warmup + K - 1) + 1],
+            "storage": bn.storage,
+            "kv_cache_bytes_per_layer": 2 * bn.case.k_cache[0].numel()
+            * bn.case.k_cache.element_size()})
+    dec.close()
+    del cap, dec
+    torch.cuda.synchronize()
+    return res, bn, clocks
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+
+    import dynamic_sparse_kv_gb300  # noqa: F401  (loads libfastocr.so or raises)
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    K, W = args.steps, args.warmup
+
+    main, bn, clocks = run_workload(args, args.workload, rank, world, dev, flush, headline=True,
+                                    sampler_gpu=gpu_uuid)
+    wl = bn.wl
+    del bn
+    torch.cuda.empty_cache()
+
+    peak, peak_src = measured_peaks()
+    probe = None if args.no_probe else read_probe(dev, flush, world)
+    kernels = main["kernels"]
+    dom = max(kernels, key=lambda k: kernels[k]["us_in_step"])
+    kd = kernels[dom]
+    kname = KERNEL_NAME[dom]
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": kd["gbs"], "peak": peak,
+                "unit": "GB/s", "frac": kd["gbs"] / peak,
+                "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_src == "measured" else "fallback 6.8 TB/s",
+                "traffic": recorded_traffic(kname, wl.name),
+                "us_per_launch_in_step": kd["us_per_layer"],
+                "launches_times_us_over_step": kd["us_in_step"] / main["us_per_step"],
+                "how": "algorithmic K/V bytes of the kind's layers / time of those layers "
+                       "replayed alone in step order (CUDA graph, L2 flushed)"}
+    if dom == "focal":
+        roofline["note"] = "a focal layer is the attend kernel plus the selection kernel"
+    if probe:
+        roofline["peak_readonly"] = probe["gbs"]
+        roofline["frac_readonly"] = kd["gbs"] / probe["gbs"]
+
+    secondary = None
+    if args.secondary and args.secondary != "none" and args.secondary != args.workload:
+        secondary, bn2, _ = run_workload(args, args.secondary, rank, world, dev, flush,
+                                         headline=False)
+        del bn2
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -503,54 +712,44 @@ def run_gpu(args, rank, world, local_rank):
             cpu = {"value": None, "unit": "steps/s", "cores": 1, "kind": "oracle",
                    "sample": f"failed: {e}"[:300]}
 
-    us_per_step = total_ms * 1e3 / K
-    step_bytes = sum(kernels[k]["kv_bytes_per_launch"] * kernels[k]["launches_per_step"]
-                     for k in kernels)
-    value = world * K / (total_ms * 1e-3)
+    us_per_step = main["us_per_step"]
+    value = world * 1e6 / us_per_step
+    config = {"workload": wl.name, "batch_per_gpu": wl.batch, "layers": wl.layers,
+              "q_heads": wl.q_heads, "kv_heads": wl.kv_heads, "head_dim": wl.head_dim,
+              "prompt": wl.prompt, "n_img": wl.n_img, "tau": wl.tau, "page_size": wl.page_size,
+              "parallelism": f"replicas{world}",
+              "l2": "flushed before every timed step (512 MB memset, untimed)"}
+    config.update({k: v for k, v in main.items() if k not in ("workload", "e2e")})
     res = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": K,
-        "warmup": W, "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-        "config": {"workload": wl.name, "batch_per_gpu": wl.batch, "layers": wl.layers,
-                   "q_heads": wl.q_heads, "kv_heads": wl.kv_heads, "head_dim": wl.head_dim,
-                   "prompt": wl.prompt, "n_img": wl.n_img, "tau": wl.tau,
-                   "focal_layers": list(focal) if focal else None, "page_size": wl.page_size,
-                   "parallelism": f"replicas{world}",
-                   "l2": "flushed before every timed step (512 MB memset, untimed)",
-                   "us_per_step": us_per_step, "kv_bytes_per_step": step_bytes,
-                   "achieved_step_gbs": step_bytes / (us_per_step * 1e-6) / 1e9,
-                   "wall_s_timed_loop": wall, "kernels": kernels, **compare},
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": cap.launches * K, "clocks": clocks,
+        "warmup": W, "ms_per_step": us_per_step * 1e-3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": config, "roofline": roofline, "read_probe": probe, "cpu_baseline": cpu,
+        "e2e": main["e2e"], "gpu_launches": main["gpu_launches_per_step"] * K,
+        "clocks": clocks, "secondary": secondary,
     }
-    if wl.mode == "rswa":
-        res["config"].update({
-            "rswa_prefix": wl.rswa_prefix, "rswa_window": wl.rswa_window,
-            "generated_tokens_timed": [t_of(W) + 1, t_of(W + K - 1) + 1], "storage": storage,
-            "kv_cache_bytes_per_layer": 2 * case.k_cache[0].numel() * case.k_cache.element_size()})
-    if "dense_us_per_step" in compare:
-        res["config"]["speedup_vs_dense"] = compare["dense_us_per_step"] / us_per_step
-        res["config"]["speedup_vs_tau1"] = compare["tau1_us_per_step"] / us_per_step
-    dec.close()
     return res
 
 
 def run_reference(args):
+    """The reference arm: the fp64 oracle on the host cores, on a bounded
+    sample of the same workload, reported with the same steps and config keys."""
     import synth
     wl = synth.workload(args.workload)
+    tau = args.tau or wl.tau
     t0 = time.perf_counter()
     legs = [run_oracle_leg(args.workload, args.tau, 3.0) for _ in range(max(1, args.steps // 50))]
     el = time.perf_counter() - t0
     v = statistics.fmean(l["value"] for l in legs)
-    steps = sum(l["steps"] for l in legs)
-    sample = (f"fp64 NumPy oracle, 1 thread, {steps} steady decode steps of sequence 0 "
+    done = sum(l["steps"] for l in legs)
+    sample = (f"fp64 NumPy oracle, 1 thread, {done} steady decode steps of sequence 0 "
               f"over {len(legs)} runs, scaled to the {wl.batch}-sequence step")
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": 0,
-            "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 / v,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / v,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "batch": wl.batch, "tau": args.tau or wl.tau,
-                       "wall_s": el},
+            "config": {"workload": wl.name, "batch_per_gpu": wl.batch, "tau": tau,
+                       "oracle_steps_timed": done, "wall_s": el},
             "cpu_baseline": {"value": v, "unit": "steps/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0,

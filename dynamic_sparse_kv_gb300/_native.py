@@ -70,6 +70,7 @@ def _load() -> ctypes.CDLL:
         "fastocr_device_status": ([P, ctypes.POINTER(I32), P], I32),
         "fastocr_set_splits": ([P, I32, I32], I32),
         "fastocr_set_length_hint": ([P, I32], I32),
+        "fastocr_read_probe": ([P, ctypes.c_int64, P, P], I32),
         "fastocr_focal_attend_noalloc": ([ctypes.POINTER(fastocr_dims), P,
                                           ctypes.POINTER(fastocr_kv), P, F64, P, P, I32, P, P, P],
                                          I32),
@@ -198,3 +199,9 @@ def fastocr_focal_attend_noalloc(dims: fastocr_dims, q, kv: fastocr_kv, img_rang
                                             _ptr(img_range), float(tau), _ptr(out), _ptr(idx),
                                             int(idx_stride), _ptr(k_out), _ptr(status),
                                             _stream(stream)))
+
+
+def fastocr_read_probe(src, nbytes, sink, stream=None) -> None:
+    """Read nbytes of device memory at src once (read-only bandwidth probe)."""
+    _check("fastocr_read_probe",
+           lib.fastocr_read_probe(_ptr(src), int(nbytes), _ptr(sink), _stream(stream)))

@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfastocr.so")
 
-SOURCES = ["abi.cu", "kernels_bf16.cu", "kernels_f32.cu", "noalloc.cu"]
+SOURCES = ["abi.cu", "kernels_bf16.cu", "kernels_f32.cu", "noalloc.cu", "probe.cu"]
 HEADERS = ["attend_kernels.cuh", "attend_impl.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

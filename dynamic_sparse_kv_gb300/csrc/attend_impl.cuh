@@ -735,11 +735,16 @@ __global__ void __launch_bounds__(32 * warps_for(ST), 2) attend_kernel(const Par
     const float b1f = sm_.m[1] == kNegInf ? 0.f : sm_.m[1];
     const float p0 = fast_exp2(s0 - b0f), p2 = fast_exp2(s2 - b0f);
     const float p1 = fast_exp2(s1 - b1f), p3 = fast_exp2(s3 - b1f);
-    sm_.l[0] += p0 + p2;
-    sm_.l[1] += p1 + p3;
+    // The P.V product takes the probabilities rounded to bf16; the softmax
+    // sum adds those same rounded values, so the weights that multiply V sum
+    // to exactly 1 after normalisation (rounding moves a weight by at most
+    // 2^-9 relative, but never the total).
+    const uint32_t pk01 = pack_bf16(p0, p1), pk23 = pack_bf16(p2, p3);
+    sm_.l[0] += __uint_as_float(pk01 << 16) + __uint_as_float(pk23 << 16);
+    sm_.l[1] += __uint_as_float(pk01 & 0xffff0000u) + __uint_as_float(pk23 & 0xffff0000u);
     // P^T[16 keys x 8 heads] as the B operand: transpose the two 8x8 blocks
-    const uint32_t bb0 = movmatrix_trans(pack_bf16(p0, p1));
-    const uint32_t bb1 = movmatrix_trans(pack_bf16(p2, p3));
+    const uint32_t bb0 = movmatrix_trans(pk01);
+    const uint32_t bb1 = movmatrix_trans(pk23);
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) {
       uint32_t a[4];
@@ -1111,8 +1116,11 @@ __global__ void __launch_bounds__(32 * warps_for(ST), 2) attend_kernel(const Par
 }
 
 // Launch with programmatic dependent launch: the grid may be scheduled while
-// the previous kernel on the stream finishes its epilogue; it waits for that
-// kernel's completion (griddepcontrol.wait) before reading any global memory.
+// the previous kernel on the stream is still running. Before its
+// griddepcontrol.wait it reads only what the previous kernel cannot be
+// writing (lengths, block table, image range, K/V rows of earlier tokens)
+// and, speculatively, the selection; q, the selection it keeps and the
+// current token's K/V are read after the wait.
 // A focal layer is two launches: the attend kernel, then the selection kernel.
 template <typename T, int D, int MODE, int ST>
 cudaError_t launch_attend(const Params& p, cudaStream_t stream) {

@@ -248,18 +248,23 @@ class CapturedStep:
     step's queries into q (and N_t into dec.seq_len), then replay(). kind:
     "fastocr" (steady FastOCR step), "dense" (full attention in every layer),
     "profile" (a profiling step: full attention with scoring, selection and
-    profile accumulation in every layer) or "rswa".
+    profile accumulation in every layer) or "rswa"; or any name with `fn`, a
+    callable fn(q, out, stream) that issues the calls (e.g. a subset of the
+    step's layers), and `launches`, the kernels it launches.
     """
 
-    def __init__(self, dec: DecodeAttention, kind: str = "fastocr"):
+    def __init__(self, dec: DecodeAttention, kind: str = "fastocr", fn=None,
+                 launches: int | None = None):
         self.dec, self.kind = dec, kind
         shape = (dec.layers, dec.batch, dec.q_heads, dec.head_dim)
         self.q = torch.zeros(shape, dtype=dec.k_cache.dtype, device=dec.k_cache.device)
         self.out = torch.zeros_like(self.q)
         if kind == "profile" and dec.warm_idx is None:
             dec.begin_warmup()
-        fn = {"fastocr": dec.step, "dense": dec.dense_step, "rswa": dec.rswa_step,
-              "profile": dec.warmup_step}[kind]
+        if fn is None:   # otherwise fn(q, out, stream) issues the calls and `launches` counts them
+            fn = {"fastocr": dec.step, "dense": dec.dense_step, "rswa": dec.rswa_step,
+                  "profile": dec.warmup_step}[kind]
+            launches = dec.launches_per_step(kind)
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
@@ -268,7 +273,7 @@ class CapturedStep:
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph):
             fn(self.q, self.out)
-        self.launches = dec.launches_per_step(kind)
+        self.launches = launches
 
     def replay(self):
         self.graph.replay()

@@ -210,6 +210,17 @@ fastocr_status fastocr_set_length_hint(fastocr_handle* h, int32_t n_t);
  * cluster) and to the largest cluster the device co-schedules. */
 fastocr_status fastocr_set_splits(fastocr_handle* h, int32_t mode, int32_t splits);
 
+/* Measurement utility, not a step of the method: read `bytes` (a multiple
+ * of 16, >= 16) of device memory at `src` (16-byte aligned) exactly once with
+ * streaming loads that bypass L1, in one kernel on `stream`, folding the data
+ * into a value that may be ORed into *sink (device uint32, caller-owned; its
+ * content is meaningless). Timed with events around it on a buffer much
+ * larger than L2, it gives the read-only HBM bandwidth that bounds the attend
+ * kernels, which only read the K/V cache. Asynchronous; allocates nothing.
+ * Errors: NULL, INVALID (size), ALIGN, NO_DEVICE, CUDA. */
+fastocr_status fastocr_read_probe(const void* src, int64_t bytes, uint32_t* sink,
+                                  fastocr_stream stream);
+
 /* Allocation-free focal layer. The pages describe no such call; it exists
  * for callers that may not allocate GPU memory at the point where they run
  * attention -- for example code living inside another framework's memory

@@ -19,3 +19,16 @@ def build_library(force=False):
     mod = importlib.util.module_from_spec(spec)
     spec.loader.exec_module(mod)
     return mod.build(force=force)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Write the per-test maximum output errors (tests/gpu_harness.py) to the
+    JSON file FASTOCR_ERR_LOG names, if it is set and any were recorded."""
+    path = os.environ.get("FASTOCR_ERR_LOG")
+    mod = sys.modules.get("gpu_harness")
+    if not path or mod is None or not mod.ERRORS:
+        return
+    import json
+    with open(path, "w") as f:
+        json.dump({k: {"max_abs_err": v[0], "max_abs_err_vs_rounded_oracle": v[1], "dtype": v[2]}
+                   for k, v in sorted(mod.ERRORS.items())}, f, indent=1)

@@ -41,11 +41,43 @@ def test_kv_bytes_rswa_equal_oracle_attend_sets(steps):
 
 
 def test_recorded_traffic_needs_matching_digest(tmp_path, monkeypatch):
-    f = tmp_path / "traffic.md"
+    import json
+    f = tmp_path / "traffic.json"
     dig = bench.source_digest()
-    f.write_text(f"`traffic attend_sparse qwen7b_b1 12345 {dig}`\n"
-                 f"`traffic attend_focal qwen7b_b1 999 0000000000000000`\n")
+    f.write_text(json.dumps({"entries": [
+        {"kernel": "attend_sparse", "workload": "qwen7b_b1", "bytes_per_launch": 12345,
+         "digest": dig},
+        {"kernel": "attend_focal", "workload": "qwen7b_b1", "bytes_per_launch": 999,
+         "digest": "0000000000000000"}]}))
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
     assert bench.recorded_traffic("attend_sparse", "qwen7b_b1") == 12345.0
     assert bench.recorded_traffic("attend_focal", "qwen7b_b1") is None      # stale digest
     assert bench.recorded_traffic("attend_rswa", "rswa_b16") is None        # not recorded
+
+
+def test_committed_traffic_file_parses():
+    import json
+    with open(bench.TRAFFIC_FILE) as f:
+        entries = json.load(f)["entries"]
+    for e in entries:
+        assert e["kernel"] in bench.KERNEL_NAME.values() and e["bytes_per_launch"] > 0
+        assert len(e["digest"]) == 16 and e["source"].startswith("profiles/")
+
+
+def test_kinds_check_flags_shares_above_the_step():
+    ok = bench.kinds_check({"focal": {"us_in_step": 300.0}, "sparse": {"us_in_step": 290.0}}, 600.0)
+    assert not ok["kinds_exceed_step"] and abs(ok["kinds_sum_over_step"] - 590 / 600) < 1e-12
+    bad = bench.kinds_check({"focal": {"us_in_step": 300.0}, "sparse": {"us_in_step": 400.0}},
+                            600.0)
+    assert bad["kinds_exceed_step"]
+
+
+def test_reference_arm_echoes_steps_and_config(monkeypatch):
+    legs = iter([{"value": 2.0, "steps": 7}])
+    monkeypatch.setattr(bench, "run_oracle_leg", lambda *a, **k: next(legs))
+    args = bench.parse_args(["--impl", "reference", "--steps", "20", "--warmup", "5"])
+    r = bench.run_reference(args)
+    assert r["steps"] == 20 and r["warmup"] == 5 and r["impl"] == "reference"
+    assert r["config"]["workload"] == args.workload == "serving_b32"
+    assert r["config"]["tau"] == synth.workload("serving_b32").tau
+    assert r["config"]["batch_per_gpu"] == 32

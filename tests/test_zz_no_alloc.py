@@ -6,14 +6,18 @@ memory pool, plugins that may not call cudaMalloc once started, loops that
 must not take the driver's allocation locks). It keeps its scratch in a
 fixed array inside the library instead of a handle's workspace. Two calls in
 a row (different steps, so the second overwrites the first call's scratch)
-must each give the same outputs and selection as fastocr_focal_attend.
+must each give the same outputs and selection as fastocr_focal_attend, and
+match the fp64 oracle on their own (outputs within the test tolerance,
+selections exact up to ties within 1e-5 of the k-th score).
 
 This file is collected last on purpose and also passes on its own.
 """
 import pytest
 import torch
 
+import oracle.attention as A
 import synth
+from gpu_harness import KVCache, assert_close, check_selection, np64
 
 pytestmark = pytest.mark.gpu
 
@@ -64,7 +68,18 @@ def test_noalloc_matches_handle_path(name, overrides):
             assert torch.equal(idx[b, :int(k[b])], idx_ref[b, :int(k_ref[b])])
         err = (out.double() - out_ref.double()).abs().max().item()
         assert err <= tol, (t, err)
+        # and each call on its own against the fp64 oracle
+        n_t = wl.seq_len_at(t)
+        kv = KVCache(case)
+        for b in range(wl.batch):
+            K, V = kv(layer, b)
+            ref_out, ref_sel, sigma = A.focal_attend(np64(q[b]), K, V, n_t, wl.prompt, wl.n_img,
+                                                     wl.tau)
+            assert_close(out[b], ref_out, tol, f"no-alloc t={t} b={b}")
+            check_selection(idx[b, :int(k[b])].cpu().numpy(), ref_sel, sigma, wl.prompt,
+                            f"no-alloc t={t} b={b}")
     assert int(status.item()) == 0
+    assert dec.device_status() == 0
     dec.close()
 
 
