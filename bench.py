@@ -137,12 +137,6 @@ def recorded_traffic(kernel: str, workload: str):
     return None
 
 
-def median_index(xs):
-    """Index of the median element (lower median)."""
-    order = sorted(range(len(xs)), key=lambda i: xs[i])
-    return order[(len(xs) - 1) // 2]
-
-
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
 
@@ -336,11 +330,14 @@ class Bench:
         self.wl = wl = wl.with_(seed=wl.seed + 1000 * rank)
         K, W = args.steps, args.warmup
         if wl.mode == "fastocr":
-            self.t0_steady, step0 = wl.warmup, 0        # the warm-up reads steps [0, warmup)
+            # queries of every decode step: the warm-up reads [0, warmup), the
+            # timed steps sample the whole steady decode (lists grow with t)
+            self.t0_steady, step0 = wl.warmup, 0
+            self.n_gen = wl.steps
         else:   # R-SWA: the last steps before T = wl.steps generated tokens (window full)
             self.t0_steady = step0 = max(0, wl.steps - (W + K))
+            self.n_gen = wl.steps - step0
         self.span = wl.steps - self.t0_steady        # steady steps available in the workload
-        self.n_gen = min(wl.steps, self.t0_steady + W + K) - step0
         case = synth.make_case(wl, device=dev, step0=step0, n_steps=self.n_gen)
         self.storage = "full"
         if wl.mode == "rswa" and args.rswa_ring:
@@ -359,8 +356,13 @@ class Bench:
         self.case = case
         self.kind = "rswa" if wl.mode == "rswa" else "fastocr"
 
-    def t_of(self, i):                       # i-th bench step -> decode step index
-        return self.t0_steady + (i % min(self.span, self.n_gen - (self.t0_steady - self.case.step0)))
+    def t_of(self, i):
+        """Decode step of the i-th bench step: every K consecutive bench steps
+        sample the steady decode at a stride of span/K steps (each group of K
+        shifted by one), so every timed pass sees the same mix of cache lengths."""
+        K = self.args.steps
+        j, p = i % K, i // K
+        return self.t0_steady + (j * self.span // K + p) % self.span
 
     def build(self, tau, kind):
         from dynamic_sparse_kv_gb300 import CapturedStep, DecodeAttention

@@ -63,6 +63,8 @@ def _load() -> ctypes.CDLL:
         "fastocr_full_attend": ([P, P, ctypes.POINTER(fastocr_kv), P, P], I32),
         "fastocr_focal_attend": ([P, P, ctypes.POINTER(fastocr_kv), P, F64, P, P, I32, P, I32, P],
                                  I32),
+        "fastocr_focal_scores": ([P, P, ctypes.POINTER(fastocr_kv), P, P, P, I32, P], I32),
+        "fastocr_select": ([P, ctypes.POINTER(fastocr_kv), P, P, I32, F64, P, I32, P, P], I32),
         "fastocr_sparse_attend": ([P, P, ctypes.POINTER(fastocr_kv), P, P, I32, P, P, P], I32),
         "fastocr_rswa_attend": ([P, P, ctypes.POINTER(fastocr_kv), I32, I32, P, P], I32),
         "fastocr_profiler_reset": ([P, P], I32),
@@ -143,6 +145,21 @@ def fastocr_focal_attend(handle, q, kv: fastocr_kv, img_range, tau, out, idx, id
            lib.fastocr_focal_attend(handle, _ptr(q), ctypes.byref(kv), _ptr(img_range),
                                     float(tau), _ptr(out), _ptr(idx), int(idx_stride),
                                     _ptr(k_out), int(profile_layer), _stream(stream)))
+
+
+def fastocr_focal_scores(handle, q, kv: fastocr_kv, img_range, out, sigma, sigma_stride,
+                         stream=None) -> None:
+    _check("fastocr_focal_scores",
+           lib.fastocr_focal_scores(handle, _ptr(q), ctypes.byref(kv), _ptr(img_range), _ptr(out),
+                                    _ptr(sigma), int(sigma_stride), _stream(stream)))
+
+
+def fastocr_select(handle, kv: fastocr_kv, img_range, sigma, sigma_stride, tau, idx, idx_stride,
+                   k_out, stream=None) -> None:
+    _check("fastocr_select",
+           lib.fastocr_select(handle, ctypes.byref(kv), _ptr(img_range), _ptr(sigma),
+                              int(sigma_stride), float(tau), _ptr(idx), int(idx_stride),
+                              _ptr(k_out), _stream(stream)))
 
 
 def fastocr_sparse_attend(handle, q, kv: fastocr_kv, img_range, idx, idx_stride, k, out,

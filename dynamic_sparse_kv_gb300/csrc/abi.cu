@@ -13,6 +13,7 @@
 namespace fastocr {
 cudaError_t launch_bf16(int head_dim, int mode, const Params& p, cudaStream_t s);
 cudaError_t launch_f32(int head_dim, int mode, const Params& p, cudaStream_t s);
+cudaError_t launch_select(const Params& p, cudaStream_t s);
 cudaError_t prepare_bf16();
 cudaError_t prepare_f32();
 int max_cluster_bf16(int head_dim);
@@ -101,6 +102,10 @@ Params base_params(const fastocr_handle* h, const void* q, const fastocr_kv* kv,
   p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d.head_dim));
   p.logits = h->logits;
   p.sigma_part = h->sigma_part;
+  p.sel_src = h->sigma_part;   // the selection sums the KV heads' score shares
+  p.sel_heads = d.num_kv_heads;
+  p.sel_head_stride = d.max_img_tokens;
+  p.sel_batch_stride = (long)d.num_kv_heads * d.max_img_tokens;
   p.profile = h->profile;
   p.profile_layer = -1;
   p.status = h->status;
@@ -249,6 +254,55 @@ fastocr_status fastocr_focal_attend(fastocr_handle* h, const void* q, const fast
   p.profile_layer = profile_layer;
   p.splits = splits_for(h, 0, expected_tokens(h));
   return launch(h, kFocal, p, stream);
+}
+
+fastocr_status fastocr_focal_scores(fastocr_handle* h, const void* q, const fastocr_kv* kv,
+                                    const int32_t* img_range, void* out, float* sigma,
+                                    int32_t sigma_stride, fastocr_stream stream) {
+  if (!h || !q || !out || !img_range || !sigma) return FASTOCR_ERR_NULL;
+  fastocr_status st = check_kv(h, kv);
+  if (st != FASTOCR_OK) return st;
+  if (!aligned16(q) || !aligned16(out)) return FASTOCR_ERR_ALIGN;
+  if (h->dims.max_img_tokens < 1 || sigma_stride < h->dims.max_img_tokens)
+    return FASTOCR_ERR_INVALID;
+  Params p = base_params(h, q, kv, out);
+  p.img_range = img_range;
+  p.tau = 1.0;
+  p.sigma_out = sigma;
+  p.sigma_stride = sigma_stride;
+  p.splits = splits_for(h, 0, expected_tokens(h));
+  return launch(h, kFocal, p, stream);
+}
+
+fastocr_status fastocr_select(fastocr_handle* h, const fastocr_kv* kv, const int32_t* img_range,
+                              const float* sigma, int32_t sigma_stride, double tau, int32_t* idx,
+                              int32_t idx_stride, int32_t* k_out, fastocr_stream stream) {
+  if (!h || !kv || !kv->seq_len || !img_range || !sigma || !idx || !k_out)
+    return FASTOCR_ERR_NULL;
+  if (!(tau > 0.0 && tau <= 1.0)) return FASTOCR_ERR_INVALID;
+  if (h->dims.max_img_tokens < 1 || sigma_stride < h->dims.max_img_tokens)
+    return FASTOCR_ERR_INVALID;
+  if (idx_stride < keep_count(tau, h->dims.max_img_tokens)) return FASTOCR_ERR_INVALID;
+  Params p;
+  memset(&p, 0, sizeof(p));
+  p.seq_len = kv->seq_len;
+  p.max_pages = h->dims.max_pages_per_seq;
+  p.log2_page = h->log2_page;
+  p.B = h->dims.batch;
+  p.img_range = img_range;
+  p.tau = tau;
+  p.idx_out = idx;
+  p.idx_stride = idx_stride;
+  p.k_out = k_out;
+  p.sel_src = sigma;
+  p.sel_heads = 1;
+  p.sel_head_stride = 0;
+  p.sel_batch_stride = sigma_stride;
+  p.profile_layer = -1;
+  p.status = h->status;
+  p.max_img = h->dims.max_img_tokens;
+  return launch_select(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FASTOCR_OK
+                                                                            : FASTOCR_ERR_CUDA;
 }
 
 fastocr_status fastocr_sparse_attend(fastocr_handle* h, const void* q, const fastocr_kv* kv,

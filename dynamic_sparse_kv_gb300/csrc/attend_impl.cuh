@@ -25,9 +25,11 @@ struct SelectSmem {
 
 // Selection kernel of a focal layer: one CTA of NT threads per sequence,
 // launched right after the focal attend kernel, which left each KV head's
-// share of the image scores in the workspace. It sums the shares into keys in
+// share of the image scores in the workspace (or on its own, on scores a
+// caller supplies). It sums the shares into keys in
 // a fixed head order, adds the image mass to the profiler slot (warm-up only),
-// and selects the k largest keys (ties to the lower offset) with an 8-bit
+// then either writes the summed scores out (sigma_out) or
+// selects the k largest keys (ties to the lower offset) with an 8-bit
 // radix select over the fp32 bit patterns (scores are >= 0, so the unsigned
 // order is the float order); the first pass is counted while the keys are
 // summed, and the search stops as soon as every key sharing the decided prefix
@@ -60,23 +62,25 @@ __global__ void __launch_bounds__(NT) select_kernel(const Params p) {
   const bool profiling = p.profile_layer >= 0;
   double local = 0.0;
   int* h0 = hist + (warp & (kSelSub - 1)) * 256;
-  const float* sp_b = p.sigma_part + (size_t)b * p.Hkv * p.max_img;
+  const float* sp_b = p.sel_src + (size_t)b * p.sel_batch_stride;
+  float* so_b = p.sigma_out ? p.sigma_out + (size_t)b * p.sigma_stride : nullptr;
   for (int i0 = 0; i0 < n; i0 += 4 * NT) {
     float sv[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int hk0 = 0; hk0 < p.Hkv; hk0 += 4) {   // 16 loads in flight, summed in head order
+    for (int hk0 = 0; hk0 < p.sel_heads; hk0 += 4) {   // 16 loads in flight, summed in head order
       float v[4][4];
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int i = i0 + u * NT + tid;
-          v[c][u] = (hk0 + c < p.Hkv && i < n) ? __ldcg(sp_b + (size_t)(hk0 + c) * p.max_img + i) : 0.f;
+          v[c][u] = (hk0 + c < p.sel_heads && i < n)
+                        ? __ldcg(sp_b + (size_t)(hk0 + c) * p.sel_head_stride + i) : 0.f;
         }
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          if (hk0 + c < p.Hkv) sv[u] += v[c][u];
+          if (hk0 + c < p.sel_heads) sv[u] += v[c][u];
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -88,6 +92,7 @@ __global__ void __launch_bounds__(NT) select_kernel(const Params p) {
       if (act) {
         keys[i] = key;
         if (profiling) local += (double)sv[u];
+        if (so_b) so_b[i] = sv[u];
       }
       if (act) atomicAdd(h0 + (key >> 24), 1);
     }
@@ -97,13 +102,14 @@ __global__ void __launch_bounds__(NT) select_kernel(const Params p) {
     for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
     if (lane == 0) dscr[warp] = local;
   }
-  if (tid == 0) p.k_out[b] = scratch[2];
+  if (tid == 0 && !so_b) p.k_out[b] = scratch[2];
   __syncthreads();
   if (profiling && tid == 0) {
     double tot = 0.0;
     for (int w = 0; w < NW; ++w) tot += dscr[w];
     atomicAdd(p.profile + p.profile_layer, tot);
   }
+  if (so_b) return;   // scores only: the caller selects (e.g. after summing head shards)
   const int k = scratch[2];
   if (k == 0) return;
 
@@ -233,6 +239,7 @@ __global__ void __launch_bounds__(NT) select_kernel(const Params p) {
 }
 
 inline int select_smem_bytes(int max_img) { return SelectSmem::bytes(max_img); }
+
 
 inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, int smem, cudaStream_t stream,
                                      cudaLaunchAttribute* attr) {
@@ -735,13 +742,20 @@ __global__ void __launch_bounds__(32 * warps_for(ST), 2) attend_kernel(const Par
     const float b1f = sm_.m[1] == kNegInf ? 0.f : sm_.m[1];
     const float p0 = fast_exp2(s0 - b0f), p2 = fast_exp2(s2 - b0f);
     const float p1 = fast_exp2(s1 - b1f), p3 = fast_exp2(s3 - b1f);
-    // The P.V product takes the probabilities rounded to bf16; the softmax
-    // sum adds those same rounded values, so the weights that multiply V sum
-    // to exactly 1 after normalisation (rounding moves a weight by at most
-    // 2^-9 relative, but never the total).
+    // The P.V product takes the probabilities rounded to bf16. Outside focal
+    // layers the softmax sum adds those same rounded values, so the weights
+    // that multiply V sum to exactly 1 after normalisation (rounding moves a
+    // weight by at most 2^-9 relative, never the total). A focal layer's sum
+    // also turns its logits into the image scores, which must be the
+    // probabilities themselves, so there it adds the unrounded values.
     const uint32_t pk01 = pack_bf16(p0, p1), pk23 = pack_bf16(p2, p3);
-    sm_.l[0] += __uint_as_float(pk01 << 16) + __uint_as_float(pk23 << 16);
-    sm_.l[1] += __uint_as_float(pk01 & 0xffff0000u) + __uint_as_float(pk23 & 0xffff0000u);
+    if (MODE == kFocal) {
+      sm_.l[0] += p0 + p2;
+      sm_.l[1] += p1 + p3;
+    } else {
+      sm_.l[0] += __uint_as_float(pk01 << 16) + __uint_as_float(pk23 << 16);
+      sm_.l[1] += __uint_as_float(pk01 & 0xffff0000u) + __uint_as_float(pk23 & 0xffff0000u);
+    }
     // P^T[16 keys x 8 heads] as the B operand: transpose the two 8x8 blocks
     const uint32_t bb0 = movmatrix_trans(pk01);
     const uint32_t bb1 = movmatrix_trans(pk23);
@@ -1138,6 +1152,14 @@ cudaError_t launch_attend(const Params& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg2 = pdl_config(dim3(p.B, 1, 1), dim3(kSelectThreads, 1, 1),
                                        select_smem_bytes(p.max_img), stream, attr2);
   return cudaLaunchKernelEx(&cfg2, select_kernel<kSelectThreads>, p);
+}
+
+// The selection kernel on its own, on the scores p.sel_src describes.
+inline cudaError_t launch_select_kernel(const Params& p, cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(p.B, 1, 1), dim3(kSelectThreads, 1, 1),
+                                      select_smem_bytes(p.max_img), stream, attr);
+  return cudaLaunchKernelEx(&cfg, select_kernel<kSelectThreads>, p);
 }
 
 // Raise the dynamic shared-memory limits once per device, before any launch

@@ -80,6 +80,14 @@ struct Params {
   // workspace
   float* logits;             // [B, H_kv, max_img, kSlots]
   float* sigma_part;         // [B, H_kv, max_img]
+  // selection kernel: the score of image token i of sequence b is
+  // sum over c < sel_heads of sel_src[b*sel_batch_stride + c*sel_head_stride + i]
+  // (the KV heads' shares in the workspace, or a caller's scores)
+  const float* sel_src;
+  int sel_heads;
+  long sel_head_stride, sel_batch_stride;
+  float* sigma_out;          // set: write the summed scores [B, sigma_stride] and select nothing
+  int sigma_stride;
   double* profile;           // [num_layers]
   int profile_layer;
   int pdl_early;             // grid fits on the SMs next to the next one: trigger it at once

@@ -25,6 +25,10 @@ int max_cluster_deep_f32(int head_dim) {
                         : max_cluster_size<float, 128, kStagesDeep>();
 }
 
+// The selection kernel does not depend on the cache dtype; this unit hosts
+// its stand-alone launch.
+cudaError_t launch_select(const Params& p, cudaStream_t s) { return launch_select_kernel(p, s); }
+
 int active_clusters_f32(int head_dim, int cluster) {
   return head_dim == 64 ? active_clusters<float, 64>(cluster) : active_clusters<float, 128>(cluster);
 }

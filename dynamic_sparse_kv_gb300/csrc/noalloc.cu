@@ -152,6 +152,10 @@ extern "C" fastocr_status fastocr_focal_attend_noalloc(
   // call, so the scratch needs no clearing between calls
   p.logits = st->scratch;
   p.sigma_part = st->scratch + units_img * kSlots;
+  p.sel_src = p.sigma_part;   // the selection sums the KV heads' score shares
+  p.sel_heads = d.num_kv_heads;
+  p.sel_head_stride = d.max_img_tokens;
+  p.sel_batch_stride = (long)d.num_kv_heads * d.max_img_tokens;
   p.profile = nullptr;
   p.profile_layer = -1;
   p.status = status;

@@ -99,7 +99,7 @@ class DecodeAttention:
 
     def __init__(self, k_cache, v_cache, block_table, *, q_heads: int, img_range=None,
                  max_img: int = 0, tau: float = 1.0, mode: str = "fastocr",
-                 rswa_prefix: int = 0, rswa_window: int = 0, splits=None):
+                 rswa_prefix: int = 0, rswa_window: int = 0, splits=None, score_reduce=None):
         assert k_cache.is_cuda and k_cache.shape == v_cache.shape
         self.k_cache, self.v_cache = k_cache, v_cache
         self.layers, self.num_pages, self.kv_heads, self.page_size, self.head_dim = k_cache.shape
@@ -129,6 +129,13 @@ class DecodeAttention:
         self.warm_idx = None   # [layers, B, stride] selections made during warm-up
         self.warm_k = None
         self.has_f_last = False
+        # Head-sharded focal layers: score_reduce(sigma) sums the [B, max_img]
+        # fp32 score shares of all GPUs that hold this sequence's heads, in
+        # place (e.g. an all-reduce); focal layers then score, reduce and
+        # select in three steps instead of one call.
+        self.score_reduce = score_reduce
+        self.sigma = (torch.zeros(self.batch, max(self.max_img, 1), dtype=torch.float32,
+                                  device=dev) if score_reduce is not None else None)
 
     def close(self):
         if self.handle:
@@ -203,14 +210,25 @@ class DecodeAttention:
         return None
 
     # ------------------------------------------------------------ steps
+    def focal_layer(self, l, q_l, out_l, idx, k, stream=None):
+        """One focal layer: attention, image scores and the top-k selection."""
+        if self.score_reduce is None:
+            N.fastocr_focal_attend(self.handle, q_l, self.kv[l], self.img_range, self.tau,
+                                   out_l, idx, self.stride, k, -1, stream)
+            return
+        N.fastocr_focal_scores(self.handle, q_l, self.kv[l], self.img_range, out_l, self.sigma,
+                               self.sigma.shape[1], stream)
+        self.score_reduce(self.sigma)
+        N.fastocr_select(self.handle, self.kv[l], self.img_range, self.sigma,
+                         self.sigma.shape[1], self.tau, idx, self.stride, k, stream)
+
     def step(self, q, out, stream=None):
         """One steady FastOCR decode step over all layers (q, out: [L, B, H_q, d])."""
         cur = self.sel[max(self.focal)] if self.has_f_last else None
         for l in range(self.layers):
             if l in self.sel:
                 idx, k = self.sel[l]
-                N.fastocr_focal_attend(self.handle, q[l], self.kv[l], self.img_range, self.tau,
-                                       out[l], idx, self.stride, k, -1, stream)
+                self.focal_layer(l, q[l], out[l], idx, k, stream)
                 cur = (idx, k)
             elif cur is None:
                 N.fastocr_full_attend(self.handle, q[l], self.kv[l], out[l], stream)

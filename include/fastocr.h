@@ -162,6 +162,31 @@ fastocr_status fastocr_focal_attend(fastocr_handle* h, const void* q, const fast
                                     int32_t* idx, int32_t idx_stride, int32_t* k_out,
                                     int32_t profile_layer, fastocr_stream stream);
 
+/* Head-sharded focal layer, part 1 [FGP]: what fastocr_focal_attend computes
+ * for this handle's heads, without the selection. A sequence's heads may be
+ * split over several GPUs (tensor parallelism), each holding whole GQA
+ * groups; the image score is a sum over all query heads, so each GPU's share
+ * must be summed (an all-reduce) before the top-k, which fastocr_select then
+ * takes. Writes out (this handle's H_q heads) and sigma[b*sigma_stride + i],
+ * i < N_img_b: the image probabilities of token start_b + i summed over this
+ * handle's query heads (fp32, device, caller-owned; sigma_stride >=
+ * max_img_tokens). Entries at and beyond N_img_b are not written. */
+fastocr_status fastocr_focal_scores(fastocr_handle* h, const void* q, const fastocr_kv* kv,
+                                    const int32_t* img_range, void* out, float* sigma,
+                                    int32_t sigma_stride, fastocr_stream stream);
+
+/* Head-sharded focal layer, part 2 [FGP]: the top k_b = ceil(tau*N_img_b) of
+ * the scores sigma[b*sigma_stride + i], i < N_img_b (any non-negative fp32
+ * values, e.g. fastocr_focal_scores shares summed over all GPUs), ties to the
+ * lower position, written like fastocr_focal_attend's selection to
+ * idx[b*idx_stride ..] (ascending absolute positions) and k_out[b]. Reads
+ * kv->seq_len and img_range only (other kv fields may be NULL). Every GPU
+ * that passes the same scores gets the same selection. One kernel on stream;
+ * tau in (0, 1]; idx_stride >= ceil(tau*max_img_tokens). */
+fastocr_status fastocr_select(fastocr_handle* h, const fastocr_kv* kv, const int32_t* img_range,
+                              const float* sigma, int32_t sigma_stride, double tau, int32_t* idx,
+                              int32_t idx_stride, int32_t* k_out, fastocr_stream stream);
+
 /* Non-focal layer [FGP, CSFR]: attention over the text prefix [0, start),
  * the k[b] selected image positions idx[b*idx_stride + 0 .. k[b]-1] (any
  * order, each inside the image range), and the generated tokens

@@ -440,3 +440,80 @@ def test_length_hint_changes_speed_not_results():
             assert_close(out_s[b], A.sparse_attend(qb, Kl, Vl, n_t, wl.prompt, wl.n_img, got),
                          TOL["bf16"], f"sparse hint={hint} b={b}")
     assert dec.device_status() == 0
+
+
+def test_head_sharded_focal():
+    """Head-sharded focal layer on one GPU: two handles each own half of the KV
+    heads (whole GQA groups, as two tensor-parallel GPUs would),
+    fastocr_focal_scores gives each shard's output heads and score share, the
+    shares are summed (the all-reduce) and fastocr_select picks the top k.
+    Each shard's heads match the oracle's; the summed scores match the
+    oracle's; the selection matches the oracle's and the unsharded call's up
+    to ties within 1e-5 of the k-th score."""
+    from dynamic_sparse_kv_gb300 import _native as N
+    from dynamic_sparse_kv_gb300.sharded import shard_heads
+    case = _case("qwen7b_b1", batch=3, layers=1, prompt=40, grid=(1, 24, 24), steps=12, tau=0.05)
+    wl = case.wl
+    n_t = wl.seq_len_at(11)
+    q = case.q_at(11)[0].contiguous()
+    dec = _direct(case, n_t)
+    idx_u = torch.zeros(wl.batch, dec.stride, dtype=torch.int32, device="cuda")
+    k_u = torch.zeros(wl.batch, dtype=torch.int32, device="cuda")
+    out_u = torch.empty_like(q)
+    N.fastocr_focal_attend(dec.handle, q, dec.kv[0], case.img_range, wl.tau, out_u, idx_u,
+                           dec.stride, k_u)
+    sigma = torch.zeros(wl.batch, wl.n_img, dtype=torch.float32, device="cuda")
+    shards = []
+    for r in range(2):
+        q0, q1, kv0, kv1 = shard_heads(wl.q_heads, wl.kv_heads, r, 2)
+        k_s = case.k_cache[0][:, kv0:kv1].contiguous()
+        v_s = case.v_cache[0][:, kv0:kv1].contiguous()
+        h = N.fastocr_create(wl.batch, q1 - q0, kv1 - kv0, wl.head_dim, N.FASTOCR_DTYPE_BF16,
+                             wl.page_size, dec.block_table.shape[1], wl.n_img, 1)
+        kv = N.make_kv(k_s, v_s, dec.block_table, dec.seq_len)
+        q_s = q[:, q0:q1].contiguous()
+        out_s = torch.empty_like(q_s)
+        share = torch.full((wl.batch, wl.n_img + 3), -1.0, dtype=torch.float32, device="cuda")
+        N.fastocr_focal_scores(h, q_s, kv, case.img_range, out_s, share, share.shape[1])
+        shards.append((h, kv, (k_s, v_s), q0, q1, out_s, share))
+    for s in shards:
+        sigma += s[6][:, :wl.n_img]                 # the all-reduce of two ranks
+    idx = torch.full((wl.batch, dec.stride), -1, dtype=torch.int32, device="cuda")
+    k = torch.full((wl.batch,), -1, dtype=torch.int32, device="cuda")
+    h0, kv0_ = shards[0][0], shards[0][1]
+    N.fastocr_select(h0, kv0_, case.img_range, sigma, wl.n_img, wl.tau, idx, dec.stride, k)
+    torch.cuda.synchronize()
+    kv = KVCache(case)
+    for b in range(wl.batch):
+        Kl, Vl = kv(0, b)
+        qb = np64(q[b])
+        ref_out, ref_sel, ref_sigma = A.focal_attend(qb, Kl, Vl, n_t, wl.prompt, wl.n_img, wl.tau)
+        for (_, _, _, q0, q1, out_s, share) in shards:
+            assert_close(out_s[b], ref_out[q0:q1], TOL["bf16"], f"shard heads {q0}:{q1} b={b}")
+            assert (share[b, wl.n_img:] == -1.0).all()   # nothing written past N_img
+        got_sigma = np64(sigma[b])
+        assert np.max(np.abs(got_sigma - ref_sigma)) <= 1e-4 * np.max(ref_sigma)
+        assert int(k[b]) == A.keep_count(wl.tau, wl.n_img)
+        got = idx[b, :int(k[b])].cpu().numpy()
+        check_selection(got, ref_sel, ref_sigma, wl.prompt, f"sharded b={b}")
+        check_selection(got, idx_u[b, :int(k_u[b])].cpu().numpy(), ref_sigma, wl.prompt,
+                        f"sharded vs unsharded b={b}")
+    for s in shards:
+        assert N.fastocr_device_status(s[0]) == 0
+        N.fastocr_destroy(s[0])
+    assert dec.device_status() == 0
+
+
+def test_score_reduce_path_whole_decode():
+    """DecodeAttention with a score_reduce hook (one shard: the hook adds
+    nothing) runs its focal layers as scores -> reduce -> select; the whole
+    decode (warm-up, C, CSFR) matches the oracle like the one-call path."""
+    case = _case("qwen7b_b1", batch=2, layers=5, prompt=40, grid=(1, 16, 24), steps=12,
+                 warmup=3, n_focal=2)
+    calls = []
+    run = GpuRun(case)
+    run.dec.score_reduce = lambda sigma: calls.append(sigma.shape)
+    run.dec.sigma = torch.zeros(case.wl.batch, case.wl.n_img, dtype=torch.float32, device="cuda")
+    run.run(0, case.wl.steps)
+    compare_decode(run, case.wl.steps)
+    assert len(calls) == 2 * (case.wl.steps - case.wl.warmup)   # two focal layers a step
