@@ -71,6 +71,7 @@ def _load() -> ctypes.CDLL:
         "fastocr_profiler_select": ([P, I32, ctypes.POINTER(I32), ctypes.POINTER(F64), P], I32),
         "fastocr_device_status": ([P, ctypes.POINTER(I32), P], I32),
         "fastocr_set_splits": ([P, I32, I32], I32),
+        "fastocr_set_variant": ([P, I32, I32], I32),
         "fastocr_set_length_hint": ([P, I32], I32),
         "fastocr_read_probe": ([P, ctypes.c_int64, P, P], I32),
         "fastocr_focal_attend_noalloc": ([ctypes.POINTER(fastocr_dims), P,
@@ -202,6 +203,13 @@ def fastocr_set_length_hint(handle, n_t) -> None:
 
 def fastocr_set_splits(handle, mode, splits) -> None:
     _check("fastocr_set_splits", lib.fastocr_set_splits(handle, int(mode), int(splits)))
+
+
+VARIANT_AUTO, VARIANT_GENERAL, VARIANT_DEEP = 0, 1, 2
+
+
+def fastocr_set_variant(handle, mode, variant) -> None:
+    _check("fastocr_set_variant", lib.fastocr_set_variant(handle, int(mode), int(variant)))
 
 
 NOALLOC_MAX_UNITS_IMG = 65536   # FASTOCR_NOALLOC_MAX_UNITS_IMG

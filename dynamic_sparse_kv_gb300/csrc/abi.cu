@@ -16,10 +16,8 @@ cudaError_t launch_f32(int head_dim, int mode, const Params& p, cudaStream_t s);
 cudaError_t launch_select(const Params& p, cudaStream_t s);
 cudaError_t prepare_bf16();
 cudaError_t prepare_f32();
-int max_cluster_bf16(int head_dim);
-int max_cluster_deep_bf16(int head_dim);
-int max_cluster_deep_f32(int head_dim);
-int max_cluster_f32(int head_dim);
+int max_cluster_bf16(int head_dim, int variant);
+int max_cluster_f32(int head_dim, int variant);
 int active_clusters_bf16(int head_dim, int cluster);
 int active_clusters_f32(int head_dim, int cluster);
 }  // namespace fastocr
@@ -32,8 +30,9 @@ struct fastocr_handle {
   int num_sms;
   int log2_page;
   int split_override[3];
+  int variant_override[3];      // 0: automatic, else Variant + 1
   int max_splits;   // largest thread-block cluster the device co-schedules (<= 16)
-  int max_splits_deep;   // same for the one-CTA-per-SM variant (0: none)
+  int max_splits_v[kNumVariants];   // same per variant (0: the variant does not exist)
   int active[kMaxSplits + 1];   // clusters of each size the device holds at once
   long len_hint;    // caller's N_t of the coming calls (0: unknown), split choice only
   void* ws;
@@ -56,11 +55,27 @@ int ilog2_exact(int x) {
   return (1 << l) == x ? l : -1;
 }
 
-int splits_for(const fastocr_handle* h, int mode_slot, long len) {
-  const int o = h->split_override[mode_slot];
-  return o > 0 ? std::min(o, h->max_splits)
-               : choose_splits((long)h->dims.batch * h->dims.num_kv_heads, len, h->max_splits,
-                               h->active, h->num_sms);
+int slot_of(int mode) { return mode == kSparse ? 1 : (mode == kRswa ? 2 : 0); }
+
+// Kernel variant and split count of a launch whose attend lists hold about
+// `len` entries per (sequence, KV head) unit; caller overrides win.
+void plan_launch(const fastocr_handle* h, int mode, long len, Params& p) {
+  const int slot = slot_of(mode);
+  const long units = (long)h->dims.batch * h->dims.num_kv_heads;
+  if (len < 1) len = 1;
+  int v = h->variant_override[slot] - 1;   // -1: automatic
+  int s = h->split_override[slot];         // 0: automatic
+  if (s == 0) s = choose_splits(units, len, h->max_splits, h->active, h->num_sms);
+  // grids that leave room for the next kernel's CTAs at one CTA per SM take
+  // the deeper pipeline (more of each CTA's tiles staged before the wait)
+  if (v < 0)
+    v = (2L * s * units <= h->num_sms && s <= h->max_splits_v[kDeep]) ? kDeep : kGeneral;
+  p.variant = v;
+  p.splits = std::max(1, std::min(s, h->max_splits_v[v]));
+  // small grids release the next kernel right away (its CTAs then prefetch
+  // while this one runs); grids that need the whole GPU release it only
+  // after their main loop, so its CTAs do not take slots from this grid
+  p.pdl_early = (long)p.splits * units <= h->num_sms;
 }
 
 long max_tokens(const fastocr_handle* h) {
@@ -113,15 +128,10 @@ Params base_params(const fastocr_handle* h, const void* q, const fastocr_kv* kv,
   return p;
 }
 
-fastocr_status launch(const fastocr_handle* h, int mode, Params p, fastocr_stream stream) {
+fastocr_status launch(const fastocr_handle* h, int mode, long len, Params p,
+                      fastocr_stream stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // small grids release the next kernel right away (its CTAs then prefetch
-  // while this one runs); grids that need the whole GPU release it only
-  // after their main loop, so its CTAs do not take slots from this grid
-  p.pdl_early = (long)p.splits * p.Hkv * p.B <= h->num_sms;
-  // grids that leave room for the next kernel's CTAs at one CTA per SM take
-  // the deeper pipeline (more of each CTA's tiles staged before the wait)
-  p.deep = 2L * p.splits * p.Hkv * p.B <= h->num_sms && p.splits <= h->max_splits_deep;
+  plan_launch(h, mode, len, p);
   cudaError_t e = h->dims.dtype == FASTOCR_DTYPE_BF16 ? launch_bf16(h->dims.head_dim, mode, p, s)
                                                        : launch_f32(h->dims.head_dim, mode, p, s);
   return e == cudaSuccess ? FASTOCR_OK : FASTOCR_ERR_CUDA;
@@ -187,10 +197,10 @@ fastocr_status fastocr_create(const fastocr_dims* dims, fastocr_handle** out) {
   h->device = dev;
   h->num_sms = prop.multiProcessorCount;
   h->log2_page = log2_page;
-  h->max_splits = d.dtype == FASTOCR_DTYPE_BF16 ? max_cluster_bf16(d.head_dim)
-                                                : max_cluster_f32(d.head_dim);
-  h->max_splits_deep = d.dtype == FASTOCR_DTYPE_BF16 ? max_cluster_deep_bf16(d.head_dim)
-                                                     : max_cluster_deep_f32(d.head_dim);
+  for (int v = 0; v < kNumVariants; ++v)
+    h->max_splits_v[v] = d.dtype == FASTOCR_DTYPE_BF16 ? max_cluster_bf16(d.head_dim, v)
+                                                       : max_cluster_f32(d.head_dim, v);
+  h->max_splits = h->max_splits_v[kGeneral];
   for (int c = 1; c <= h->max_splits; ++c)
     h->active[c] = d.dtype == FASTOCR_DTYPE_BF16 ? active_clusters_bf16(d.head_dim, c)
                                                  : active_clusters_f32(d.head_dim, c);
@@ -229,8 +239,7 @@ fastocr_status fastocr_full_attend(fastocr_handle* h, const void* q, const fasto
   if (st != FASTOCR_OK) return st;
   if (!aligned16(q) || !aligned16(out)) return FASTOCR_ERR_ALIGN;
   Params p = base_params(h, q, kv, out);
-  p.splits = splits_for(h, 0, expected_tokens(h));
-  return launch(h, kFull, p, stream);
+  return launch(h, kFull, expected_tokens(h), p, stream);
 }
 
 fastocr_status fastocr_focal_attend(fastocr_handle* h, const void* q, const fastocr_kv* kv,
@@ -252,8 +261,7 @@ fastocr_status fastocr_focal_attend(fastocr_handle* h, const void* q, const fast
   p.idx_stride = idx_stride;
   p.k_out = k_out;
   p.profile_layer = profile_layer;
-  p.splits = splits_for(h, 0, expected_tokens(h));
-  return launch(h, kFocal, p, stream);
+  return launch(h, kFocal, expected_tokens(h), p, stream);
 }
 
 fastocr_status fastocr_focal_scores(fastocr_handle* h, const void* q, const fastocr_kv* kv,
@@ -270,8 +278,7 @@ fastocr_status fastocr_focal_scores(fastocr_handle* h, const void* q, const fast
   p.tau = 1.0;
   p.sigma_out = sigma;
   p.sigma_stride = sigma_stride;
-  p.splits = splits_for(h, 0, expected_tokens(h));
-  return launch(h, kFocal, p, stream);
+  return launch(h, kFocal, expected_tokens(h), p, stream);
 }
 
 fastocr_status fastocr_select(fastocr_handle* h, const fastocr_kv* kv, const int32_t* img_range,
@@ -321,8 +328,7 @@ fastocr_status fastocr_sparse_attend(fastocr_handle* h, const void* q, const fas
   p.k_in = k;
   // text tokens (cache minus the image) plus at most idx_stride selected ones
   const long text = std::max(0L, expected_tokens(h) - (long)h->dims.max_img_tokens);
-  p.splits = splits_for(h, 1, std::min(expected_tokens(h), text + idx_stride));
-  return launch(h, kSparse, p, stream);
+  return launch(h, kSparse, std::min(expected_tokens(h), text + idx_stride), p, stream);
 }
 
 fastocr_status fastocr_rswa_attend(fastocr_handle* h, const void* q, const fastocr_kv* kv,
@@ -336,8 +342,7 @@ fastocr_status fastocr_rswa_attend(fastocr_handle* h, const void* q, const fasto
   Params p = base_params(h, q, kv, out);
   p.prefix_len = prefix_len;
   p.window = window;
-  p.splits = splits_for(h, 2, std::min(expected_tokens(h), (long)prefix_len + window));
-  return launch(h, kRswa, p, stream);
+  return launch(h, kRswa, std::min(expected_tokens(h), (long)prefix_len + window), p, stream);
 }
 
 fastocr_status fastocr_profiler_reset(fastocr_handle* h, fastocr_stream stream) {
@@ -392,7 +397,15 @@ fastocr_status fastocr_set_length_hint(fastocr_handle* h, int32_t n_t) {
 fastocr_status fastocr_set_splits(fastocr_handle* h, int32_t mode, int32_t splits) {
   if (!h) return FASTOCR_ERR_NULL;
   if (mode < 0 || mode > 2 || splits < 0) return FASTOCR_ERR_INVALID;
-  h->split_override[mode] = splits == 0 ? 0 : std::min(std::max(splits, 1), h->max_splits);
+  h->split_override[mode] = splits == 0 ? 0 : std::min(std::max(splits, 1), kMaxSplits);
+  return FASTOCR_OK;
+}
+
+fastocr_status fastocr_set_variant(fastocr_handle* h, int32_t mode, int32_t variant) {
+  if (!h) return FASTOCR_ERR_NULL;
+  if (mode < 0 || mode > 2 || variant < 0 || variant > kNumVariants) return FASTOCR_ERR_INVALID;
+  if (variant > 0 && h->max_splits_v[variant - 1] == 0) return FASTOCR_ERR_UNSUPPORTED;
+  h->variant_override[mode] = variant;
   return FASTOCR_OK;
 }
 

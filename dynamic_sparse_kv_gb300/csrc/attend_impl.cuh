@@ -348,15 +348,15 @@ __device__ __forceinline__ void add_selection(const Params& p, int k, int split,
   c.n_sel = max(0, min(per, k - c.sel_lo));
 }
 
-// ST: cp.async pipeline depth per warp (kStages, or kStagesDeep for grids
-// small enough that every CTA has an SM of its own).
-template <typename T, int D, int MODE, int ST>
-__global__ void __launch_bounds__(32 * warps_for(ST), 2) attend_kernel(const Params p) {
+// V: the kernel variant (warps per CTA and cp.async stages per warp).
+template <typename T, int D, int MODE, int V>
+__global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kernel(const Params p) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  using SM = Smem<T, D, ST>;
-  constexpr int kWarps = warps_for(ST);
+  using SM = Smem<T, D, V>;
+  constexpr int ST = stages_of(V);
+  constexpr int kWarps = warps_for(V);
   constexpr int kThreads = 32 * kWarps;
-  constexpr int kSliceMax = slice_for(ST);
+  constexpr int kSliceMax = slice_for(V);
   using E = EpiSmem<D, kWarps>;
   constexpr bool kMma = sizeof(T) == 2;
   constexpr int ROWB = SM::kRowBytes;
@@ -488,6 +488,7 @@ __global__ void __launch_bounds__(32 * warps_for(ST), 2) attend_kernel(const Par
   constexpr int kPer = kSliceMax / kThreads;
   const int n_txt0 = min(n_txt_pad, kSliceMax);
   resolve(0, 0, n_txt0);
+  int pre_issued = 0;   // leading tiles of this warp already staged
   int spec_u1 = n_txt_pad;   // speculative selection entries: [n_txt_pad, spec_u1)
   int spec_raw[kPer];
   if (MODE == kSparse) {
@@ -523,9 +524,15 @@ __global__ void __launch_bounds__(32 * warps_for(ST), 2) attend_kernel(const Par
       int row = -1, ps = pos[j];
       if (ps >= 0 && page[j] >= 0 && page[j] < p.num_pages) {
         row = ((page[j] * p.Hkv + hkv) << p.log2_page) | (ps & page_mask);
-        if (u >= u_staged) {   // beyond the staged tiles: pull into L2 for later
-          prefetch_l2(kg + (size_t)row * D, ROWB);
-          prefetch_l2(vg + (size_t)row * D, ROWB);
+        // beyond the staged tiles: pull into L2 for later. Only the general
+        // variant (large grids) does: there it shortens the post-wait stream,
+        // while the deep variant's small grids measured faster without the
+        // extra traffic next to the running layer.
+        if constexpr (V == kGeneral) {
+          if (u >= u_staged) {
+            prefetch_l2(kg + (size_t)row * D, ROWB);
+            prefetch_l2(vg + (size_t)row * D, ROWB);
+          }
         }
       } else {
         ps = -1;
@@ -556,9 +563,8 @@ __global__ void __launch_bounds__(32 * warps_for(ST), 2) attend_kernel(const Par
     spos[n_pre] = ps;
   }
   __syncthreads();
-  int pre_issued = 0;   // leading tiles of this warp already staged
 #pragma unroll 1
-  for (int j = 0; j < ST; ++j) {
+  for (int j = pre_issued; j < ST; ++j) {   // then the selection's (sparse)
     const int end = (warp + j * kWarps + 1) * kTile;
     if (pre_issued == j && end <= n_pre) {
       issue(j, n_pre);
@@ -939,16 +945,17 @@ __global__ void __launch_bounds__(32 * warps_for(ST), 2) attend_kernel(const Par
   if (bad) atomicOr(p.status, bad);
   __syncthreads();
 
-  // focal: this CTA's image tokens and the logits of its first 4*kThreads of
-  // them, loaded now so that the load latency hides behind the merge
+  // focal: this CTA's image tokens and the logits of its first kSgU*kThreads
+  // of them, loaded now so that the load latency hides behind the merge
+  constexpr int kSgU = 8;   // image tokens a thread scores per round (16 loads in flight)
   const int img_end = c.img_start + c.n_img;
   // a focal text list is [0, N_t - 1): text index = position
   const int sg_lo = max(c.txt_lo, c.img_start) - c.img_start;
   const int sg_hi = min(c.txt_lo + c.n_txt, img_end) - c.img_start;
-  float4 sgx[4][2];
+  float4 sgx[kSgU][2];
   if constexpr (MODE == kFocal) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kSgU; ++u) {
       const int i = sg_lo + u * kThreads + tid;
       const float4* src4 = reinterpret_cast<const float4*>(logit_base + (size_t)i * kSlots);
       sgx[u][0] = i < sg_hi ? __ldcg(src4) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -956,19 +963,9 @@ __global__ void __launch_bounds__(32 * warps_for(ST), 2) attend_kernel(const Par
     }
   }
 
-  // ---------------- push the CTA partial to the CTAs of the cluster
-  // CTA `r` of the S splits owns output pairs [r*per, (r+1)*per) of the
-  // (head, 4 dims) pairs; every CTA writes its share of each owner's pairs,
-  // and its per-head (max, sum), straight into the owner's shared memory.
-  // The CTA partial (its W warps merged) is formed by the pushing threads
-  // themselves: a thread needs only its head's W (max, sum) pairs.
   const int S = p.splits;
-  const uint32_t rank = cluster_ctarank();
   constexpr int C4 = D / 4;
   const int n_pairs = p.g * C4;
-  const int per = (n_pairs + S - 1) / S;
-  float* rml = reinterpret_cast<float*>(smem + SM::kRecvMl);     // [S][8][2]
-  float* racc = reinterpret_cast<float*>(smem + SM::kRecvAcc);   // [S][per][4]
   auto warp_scales = [&](int h, float sc[kWarps]) -> float {   // CTA max of head h
     float M = kNegInf;
 #pragma unroll
@@ -978,66 +975,110 @@ __global__ void __launch_bounds__(32 * warps_for(ST), 2) attend_kernel(const Par
     for (int w = 0; w < kWarps; ++w) sc[w] = fast_exp2(wm[w * kSlots + h] - base);
     return M;
   };
-  const bool solo = S == 1;   // own shared memory, a CTA barrier instead of the cluster's
-  if (!solo) cluster_wait();   // every CTA of the cluster has started (its receive area exists)
-  for (int e = tid; e < S * kSlots; e += kThreads) {
-    const int r = e / kSlots, h = e % kSlots;
-    float sc[kWarps];
-    const float M = warp_scales(h, sc);
-    float L = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) L = fmaf(wl[w * kSlots + h], sc[w], L);
-    if (solo)
-      *reinterpret_cast<float2*>(rml + h * 2) = make_float2(M, L);
-    else
-      st_dsmem_f32x2(rml + (rank * kSlots + h) * 2, r, M, L);
-  }
-  for (int e = tid; e < n_pairs; e += kThreads) {
-    const int h = e / C4, c4 = e % C4;
-    float sc[kWarps];
-    warp_scales(h, sc);
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float4 v = *reinterpret_cast<const float4*>(wacc + (w * kSlots + h) * D + 4 * c4);
-      a.x = fmaf(v.x, sc[w], a.x);
-      a.y = fmaf(v.y, sc[w], a.y);
-      a.z = fmaf(v.z, sc[w], a.z);
-      a.w = fmaf(v.w, sc[w], a.w);
+  T* outp = static_cast<T*>(p.out) + ((size_t)b * p.Hq + (size_t)hkv * p.g) * D;
+  auto store_pair = [&](int e, float4 acc) {   // output dims 4*(e % C4).. of head e / C4
+    T* o = outp + (e / C4) * D + 4 * (e % C4);
+    if constexpr (kMma) {
+      uint2 w;
+      w.x = pack_bf16(acc.x, acc.y);
+      w.y = pack_bf16(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(o) = w;
+    } else {
+      *reinterpret_cast<float4*>(o) = acc;
     }
-    const int r = e / per;
-    if (solo)
-      *reinterpret_cast<float4*>(racc + (size_t)e * 4) = a;
-    else
+  };
+  float* sM = reinterpret_cast<float*>(smem + E::kM);        // focal: heads' max
+  float* sInvL = reinterpret_cast<float*>(smem + E::kInvL);  // focal: heads' 1/sum
+
+  if (S == 1) {
+    // ---------------- one CTA holds the whole list: its warps' partials
+    // merge straight into the output, in one pass after one barrier
+    for (int e = tid; e < n_pairs; e += kThreads) {
+      const int h = e / C4, c4 = e % C4;
+      float sc[kWarps];
+      warp_scales(h, sc);
+      float L = 0.f;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        L = fmaf(wl[w * kSlots + h], sc[w], L);
+        const float4 v = *reinterpret_cast<const float4*>(wacc + (w * kSlots + h) * D + 4 * c4);
+        a.x = fmaf(v.x, sc[w], a.x);
+        a.y = fmaf(v.y, sc[w], a.y);
+        a.z = fmaf(v.z, sc[w], a.z);
+        a.w = fmaf(v.w, sc[w], a.w);
+      }
+      const float inv = L > 0.f ? __frcp_rn(L) : 0.f;
+      store_pair(e, make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv));
+    }
+    if (MODE == kFocal && tid < kSlots) {
+      float sc[kWarps];
+      const float M = warp_scales(tid, sc);
+      float L = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) L = fmaf(wl[w * kSlots + tid], sc[w], L);
+      sM[tid] = M == kNegInf ? 0.f : M;
+      sInvL[tid] = L > 0.f ? __frcp_rn(L) : 0.f;
+    }
+  } else {
+    // ---------------- push the CTA partial to the CTAs of the cluster
+    // CTA `r` of the S splits owns output pairs [r*per, (r+1)*per) of the
+    // (head, 4 dims) pairs; every CTA writes its share of each owner's pairs,
+    // and its per-head (max, sum), straight into the owner's shared memory.
+    // The CTA partial (its W warps merged) is formed by the pushing threads
+    // themselves: a thread needs only its head's W (max, sum) pairs.
+    const uint32_t rank = cluster_ctarank();
+    const int per = (n_pairs + S - 1) / S;
+    float* rml = reinterpret_cast<float*>(smem + SM::kRecvMl);     // [S][8][2]
+    float* racc = reinterpret_cast<float*>(smem + SM::kRecvAcc);   // [S][per][4]
+    cluster_wait();   // every CTA of the cluster has started (its receive area exists)
+    for (int e = tid; e < S * kSlots; e += kThreads) {
+      const int r = e / kSlots, h = e % kSlots;
+      float sc[kWarps];
+      const float M = warp_scales(h, sc);
+      float L = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) L = fmaf(wl[w * kSlots + h], sc[w], L);
+      st_dsmem_f32x2(rml + (rank * kSlots + h) * 2, r, M, L);
+    }
+    for (int e = tid; e < n_pairs; e += kThreads) {
+      const int h = e / C4, c4 = e % C4;
+      float sc[kWarps];
+      warp_scales(h, sc);
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float4 v = *reinterpret_cast<const float4*>(wacc + (w * kSlots + h) * D + 4 * c4);
+        a.x = fmaf(v.x, sc[w], a.x);
+        a.y = fmaf(v.y, sc[w], a.y);
+        a.z = fmaf(v.z, sc[w], a.z);
+        a.w = fmaf(v.w, sc[w], a.w);
+      }
+      const int r = e / per;
       st_dsmem_f32x4(racc + ((size_t)rank * per + (e - r * per)) * 4, r, a);
-  }
-  if (solo)
-    __syncthreads();
-  else
+    }
     cluster_sync();   // release the pushes, acquire everyone else's
 
-  // ---------------- owner: merge the S partials of its pairs (local memory only)
-  // Each thread forms its head's max and 1/sum over the S partials itself
-  // (broadcast reads), so the merge needs no further barrier.
-  auto head_stats = [&](int h, float& base, float& inv) {
-    float ms[kMaxSplits], ls[kMaxSplits];   // all reads issued together
+    // ---------------- owner: merge the S partials of its pairs (local memory only)
+    // Each thread forms its head's max and 1/sum over the S partials itself
+    // (broadcast reads), so the merge needs no further barrier.
+    auto head_stats = [&](int h, float& base, float& inv) {
+      float ms[kMaxSplits], ls[kMaxSplits];   // all reads issued together
 #pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s) {
-      ms[s] = s < S ? rml[(s * kSlots + h) * 2] : kNegInf;
-      ls[s] = s < S ? rml[(s * kSlots + h) * 2 + 1] : 0.f;
-    }
-    float M = kNegInf;
+      for (int s = 0; s < kMaxSplits; ++s) {
+        ms[s] = s < S ? rml[(s * kSlots + h) * 2] : kNegInf;
+        ls[s] = s < S ? rml[(s * kSlots + h) * 2 + 1] : 0.f;
+      }
+      float M = kNegInf;
 #pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s) M = fmaxf(M, ms[s]);
-    base = M == kNegInf ? 0.f : M;
-    float L = 0.f;
+      for (int s = 0; s < kMaxSplits; ++s) M = fmaxf(M, ms[s]);
+      base = M == kNegInf ? 0.f : M;
+      float L = 0.f;
 #pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s) L = fmaf(ls[s], fast_exp2(ms[s] - base), L);
-    inv = L > 0.f ? __frcp_rn(L) : 0.f;
-  };
-  {
+      for (int s = 0; s < kMaxSplits; ++s) L = fmaf(ls[s], fast_exp2(ms[s] - base), L);
+      inv = L > 0.f ? __frcp_rn(L) : 0.f;
+    };
     // G adjacent lanes share one output pair, each summing every G-th partial
-    T* outp = static_cast<T*>(p.out) + ((size_t)b * p.Hq + (size_t)hkv * p.g) * D;
     const int e_lo = (int)rank * per, e_hi = min(n_pairs, e_lo + per);
     const int n_mine = max(0, e_hi - e_lo);
     int G = 1;
@@ -1047,7 +1088,7 @@ __global__ void __launch_bounds__(32 * warps_for(ST), 2) attend_kernel(const Par
          e += kThreads / G) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       const bool ok = e < e_hi;
-      const int h = ok ? e / C4 : 0, c4 = ok ? e % C4 : 0;
+      const int h = ok ? e / C4 : 0;
       if (ok) {
         float base, inv;
         head_stats(h, base, inv);
@@ -1066,27 +1107,15 @@ __global__ void __launch_bounds__(32 * warps_for(ST), 2) attend_kernel(const Par
         acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o);
         acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
       }
-      if (ok && sub == 0) {
-        T* o = outp + h * D + 4 * c4;
-        if constexpr (kMma) {
-          uint2 w;
-          w.x = pack_bf16(acc.x, acc.y);
-          w.y = pack_bf16(acc.z, acc.w);
-          *reinterpret_cast<uint2*>(o) = w;
-        } else {
-          *reinterpret_cast<float4*>(o) = acc;
-        }
-      }
+      if (ok && sub == 0) store_pair(e, acc);
     }
+    if (MODE == kFocal && tid < kSlots) head_stats(tid, sM[tid], sInvL[tid]);
   }
 
   // ---------------- focal: scores of the image tokens this CTA streamed
   // (its text share; the last CTA also the current token) from the logits it
   // wrote itself and the heads' final max and sum: no other CTA's writes read
   if constexpr (MODE == kFocal) {
-    float* sM = reinterpret_cast<float*>(smem + E::kM);
-    float* sInvL = reinterpret_cast<float*>(smem + E::kInvL);
-    if (tid < kSlots) head_stats(tid, sM[tid], sInvL[tid]);
     __syncthreads();
     float Mh[kSlots], iL[kSlots];
 #pragma unroll
@@ -1104,10 +1133,10 @@ __global__ void __launch_bounds__(32 * warps_for(ST), 2) attend_kernel(const Par
     };
     const size_t unit = (size_t)b * p.Hkv + hkv;
     float* sp = p.sigma_part + unit * p.max_img;
-    for (int i0 = sg_lo; i0 < sg_hi; i0 += 4 * kThreads) {
-      if (i0 > sg_lo) {   // later blocks of 4*kThreads tokens
+    for (int i0 = sg_lo; i0 < sg_hi; i0 += kSgU * kThreads) {
+      if (i0 > sg_lo) {   // later blocks of kSgU*kThreads tokens
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kSgU; ++u) {
           const int i = i0 + u * kThreads + tid;
           const float4* src4 = reinterpret_cast<const float4*>(logit_base + (size_t)i * kSlots);
           sgx[u][0] = i < sg_hi ? __ldcg(src4) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1115,7 +1144,7 @@ __global__ void __launch_bounds__(32 * warps_for(ST), 2) attend_kernel(const Par
         }
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kSgU; ++u) {
         const int i = i0 + u * kThreads + tid;
         const float sg = score(sgx[u][0], sgx[u][1]);
         if (i < sg_hi) sp[i] = sg;
@@ -1136,17 +1165,17 @@ __global__ void __launch_bounds__(32 * warps_for(ST), 2) attend_kernel(const Par
 // and, speculatively, the selection; q, the selection it keeps and the
 // current token's K/V are read after the wait.
 // A focal layer is two launches: the attend kernel, then the selection kernel.
-template <typename T, int D, int MODE, int ST>
+template <typename T, int D, int MODE, int V>
 cudaError_t launch_attend(const Params& p, cudaStream_t stream) {
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = pdl_config(dim3(p.splits, p.Hkv, p.B), dim3(32 * warps_for(ST), 1, 1),
-                                      attend_smem_bytes<T, D, ST>(), stream, attr);
+  cudaLaunchConfig_t cfg = pdl_config(dim3(p.splits, p.Hkv, p.B), dim3(32 * warps_for(V), 1, 1),
+                                      attend_smem_bytes<T, D, V>(), stream, attr);
   attr[1].id = cudaLaunchAttributeClusterDimension;   // the splits of one (b, hkv)
   attr[1].val.clusterDim.x = p.splits;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attend_kernel<T, D, MODE, ST>, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attend_kernel<T, D, MODE, V>, p);
   if (e != cudaSuccess || MODE != kFocal) return e;
   cudaLaunchAttribute attr2[1];
   cudaLaunchConfig_t cfg2 = pdl_config(dim3(p.B, 1, 1), dim3(kSelectThreads, 1, 1),
@@ -1177,22 +1206,22 @@ cudaError_t prepare_attend(Kern k, int bytes) {
   return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
-template <typename T, int D, int ST>
+template <typename T, int D, int V>
 cudaError_t prepare_modes() {
-  const int bytes = attend_smem_bytes<T, D, ST>();
+  const int bytes = attend_smem_bytes<T, D, V>();
   cudaError_t e;
-  if ((e = prepare_attend(attend_kernel<T, D, kFull, ST>, bytes))) return e;
-  if ((e = prepare_attend(attend_kernel<T, D, kFocal, ST>, bytes))) return e;
-  if ((e = prepare_attend(attend_kernel<T, D, kSparse, ST>, bytes))) return e;
-  return prepare_attend(attend_kernel<T, D, kRswa, ST>, bytes);
+  if ((e = prepare_attend(attend_kernel<T, D, kFull, V>, bytes))) return e;
+  if ((e = prepare_attend(attend_kernel<T, D, kFocal, V>, bytes))) return e;
+  if ((e = prepare_attend(attend_kernel<T, D, kSparse, V>, bytes))) return e;
+  return prepare_attend(attend_kernel<T, D, kRswa, V>, bytes);
 }
 
 template <typename T, int D>
 cudaError_t prepare_all_modes() {
   cudaError_t e;
-  if ((e = prepare_modes<T, D, kStages>())) return e;
-  if constexpr (deep_fits<T, D>())
-    if ((e = prepare_modes<T, D, kStagesDeep>())) return e;
+  if ((e = prepare_modes<T, D, kGeneral>())) return e;
+  if constexpr (variant_fits<T, D, kDeep>())
+    if ((e = prepare_modes<T, D, kDeep>())) return e;
   if ((e = cudaFuncSetAttribute(select_kernel<kSelectThreads>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 select_smem_bytes(kMaxImg))))
@@ -1202,13 +1231,13 @@ cudaError_t prepare_all_modes() {
                               cudaSharedmemCarveoutMaxShared);
 }
 
-// How many clusters of `c` CTAs of this kernel the device holds at once (0 if
-// a cluster of that size cannot be scheduled).
+// How many clusters of `c` CTAs of the general variant the device holds at
+// once (0 if a cluster of that size cannot be scheduled).
 template <typename T, int D>
 int active_clusters(int c) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(c, 1, 1);
-  cfg.blockDim = dim3(32 * warps_for(kStages), 1, 1);
+  cfg.blockDim = dim3(32 * warps_for(kGeneral), 1, 1);
   cfg.dynamicSmemBytes = attend_smem_bytes<T, D>();
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1218,54 +1247,67 @@ int active_clusters(int c) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, attend_kernel<T, D, kFull, kStages>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, attend_kernel<T, D, kFull, kGeneral>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   return n;
 }
 
-// Largest cluster (<= kMaxSplits) of this kernel that the device can
-// co-schedule (0: the variant does not exist).
-template <typename T, int D, int ST = kStages>
+// Largest cluster (<= kMaxSplits) of variant V that the device can
+// co-schedule (0: the variant does not exist for this dtype and head size).
+template <typename T, int D, int V>
 int max_cluster_size() {
-  if constexpr (ST == kStagesDeep && !deep_fits<T, D>()) return 0;
-  for (int c = kMaxSplits; c > 1; c >>= 1) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(c, 1, 1);
-    cfg.blockDim = dim3(32 * warps_for(ST), 1, 1);
-    cfg.dynamicSmemBytes = attend_smem_bytes<T, D, ST>();
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = c;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attend_kernel<T, D, kFull, ST>, &cfg) == cudaSuccess && n > 0)
-      return c;
-    cudaGetLastError();
+  if constexpr (!variant_fits<T, D, V>()) {
+    return 0;
+  } else {
+    for (int c = kMaxSplits; c > 1; c >>= 1) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(c, 1, 1);
+      cfg.blockDim = dim3(32 * warps_for(V), 1, 1);
+      cfg.dynamicSmemBytes = attend_smem_bytes<T, D, V>();
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = c;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, attend_kernel<T, D, kFull, V>, &cfg) == cudaSuccess && n > 0)
+        return c;
+      cudaGetLastError();
+    }
+    return 1;
   }
-  return 1;
 }
 
-template <typename T, int D, int ST>
-cudaError_t dispatch_stages(int mode, const Params& p, cudaStream_t s) {
+template <typename T, int D>
+int max_cluster_of(int variant) {
+  switch (variant) {
+    case kGeneral: return max_cluster_size<T, D, kGeneral>();
+    case kDeep: return max_cluster_size<T, D, kDeep>();
+  }
+  return 0;
+}
+
+template <typename T, int D, int V>
+cudaError_t dispatch_variant(int mode, const Params& p, cudaStream_t s) {
   switch (mode) {
-    case kFull: return launch_attend<T, D, kFull, ST>(p, s);
-    case kFocal: return launch_attend<T, D, kFocal, ST>(p, s);
-    case kSparse: return launch_attend<T, D, kSparse, ST>(p, s);
-    case kRswa: return launch_attend<T, D, kRswa, ST>(p, s);
+    case kFull: return launch_attend<T, D, kFull, V>(p, s);
+    case kFocal: return launch_attend<T, D, kFocal, V>(p, s);
+    case kSparse: return launch_attend<T, D, kSparse, V>(p, s);
+    case kRswa: return launch_attend<T, D, kRswa, V>(p, s);
   }
   return cudaErrorInvalidValue;
 }
 
 template <typename T, int D>
 cudaError_t dispatch_mode(int mode, const Params& p, cudaStream_t s) {
-  if constexpr (deep_fits<T, D>())
-    if (p.deep) return dispatch_stages<T, D, kStagesDeep>(mode, p, s);
-  return dispatch_stages<T, D, kStages>(mode, p, s);
+  if constexpr (variant_fits<T, D, kDeep>())
+    if (p.variant == kDeep) return dispatch_variant<T, D, kDeep>(mode, p, s);
+  if (p.variant != kGeneral) return cudaErrorInvalidValue;
+  return dispatch_variant<T, D, kGeneral>(mode, p, s);
 }
 
 }  // namespace fastocr

@@ -36,14 +36,17 @@ namespace fastocr {
 
 constexpr int kTile = 16;      // tokens per warp tile
 constexpr int kSlots = 8;      // query-head slots per KV head (g <= 8)
-constexpr int kStages = 2;     // cp.async pipeline depth per warp (two CTAs per SM)
-constexpr int kStagesDeep = 6; // depth of the variant for grids that leave an SM per CTA
-// Warps per CTA of each variant. The general one runs 6 warps of 2 stages:
-// with one CTA of a grid on an SM, a warp's tile loop is bound by its own
-// instruction latency, so more warps stream faster, and 12 stages still let
-// two CTAs share an SM. The deep one keeps 4 warps of 6 stages, so a
-// batch-1 CTA stages its whole share before the wait.
-__host__ __device__ constexpr int warps_for(int st) { return st == kStagesDeep ? 4 : 6; }
+// Kernel variants (warps per CTA x cp.async stages per warp):
+//  kGeneral 6 x 2: two CTAs share an SM (one of them typically the next
+//           layer's, staging its first tiles); with one CTA of a grid on an SM
+//           a warp's tile loop is bound by its own instruction latency, so
+//           more warps stream faster, and 12 stages still fit twice per SM.
+//  kDeep    4 x 6: one CTA per SM, for grids at most half the SM count; a
+//           batch-1 CTA stages its whole share before the wait.
+enum Variant : int { kGeneral = 0, kDeep = 1, kNumVariants = 2 };
+__host__ __device__ constexpr int stages_of(int v) { return v == kDeep ? 6 : 2; }
+__host__ __device__ constexpr int warps_for(int v) { return v == kDeep ? 4 : 6; }
+__host__ __device__ constexpr int ctas_per_sm(int v) { return v == kGeneral ? 2 : 1; }
 constexpr float kLazyMax = 8.f; // running-max slack (log2 units) before a rescale
 constexpr int kMaxSplits = 16;  // = the largest thread-block cluster used
 constexpr int kMaxImg = 16384; // image tokens whose scores fit in shared memory
@@ -91,7 +94,7 @@ struct Params {
   double* profile;           // [num_layers]
   int profile_layer;
   int pdl_early;             // grid fits on the SMs next to the next one: trigger it at once
-  int deep;                  // host: launch the kStagesDeep variant (one CTA per SM)
+  int variant;               // host: which Variant to launch
   int32_t* status;
   int max_img;
 };
@@ -251,12 +254,13 @@ __device__ __forceinline__ AttendList make_list(const Params& p, int b, int& bad
 
 // Work-list entries resolved to cache rows per round: a multiple of the CTA
 // size (every thread resolves the same number).
-__host__ __device__ constexpr int slice_for(int st) { return warps_for(st) == 4 ? 1024 : 960; }
+__host__ __device__ constexpr int slice_for(int v) { return v == kDeep ? 1024 : 960; }
 
-template <typename T, int D, int ST = kStages>
+template <typename T, int D, int V = kGeneral>
 struct Smem {
-  static constexpr int kWarps = warps_for(ST);
-  static constexpr int kSliceMax = slice_for(ST);
+  static constexpr int ST = stages_of(V);
+  static constexpr int kWarps = warps_for(V);
+  static constexpr int kSliceMax = slice_for(V);
   static_assert(kSliceMax % (32 * kWarps) == 0 && kSliceMax % kTile == 0, "slice layout");
   static constexpr int kRowBytes = D * (int)sizeof(T);
   static constexpr int kStageBytes = 2 * kTile * kRowBytes;          // K rows then V rows
@@ -286,17 +290,18 @@ struct EpiSmem {
   static constexpr int kBytes = kInvL + kSlots * 4;
 };
 
-template <typename T, int D, int ST = kStages>
+template <typename T, int D, int V = kGeneral>
 inline int attend_smem_bytes() {
-  static_assert(EpiSmem<D, warps_for(ST)>::kBytes <= Smem<T, D, ST>::kPipeBytes,
+  static_assert(EpiSmem<D, warps_for(V)>::kBytes <= Smem<T, D, V>::kPipeBytes,
                 "epilogue must fit the pipeline area");
-  return Smem<T, D, ST>::kMainBytes;
+  return Smem<T, D, V>::kMainBytes;
 }
 
-// The deep variant exists where its shared memory fits one CTA.
-template <typename T, int D>
-constexpr bool deep_fits() {
-  return Smem<T, D, kStagesDeep>::kMainBytes <= 227 * 1024;
+// A variant exists where its shared memory fits one CTA (the general one
+// always does; bf16 fits it twice an SM).
+template <typename T, int D, int V>
+constexpr bool variant_fits() {
+  return Smem<T, D, V>::kMainBytes <= 227 * 1024;
 }
 
 // Split-K factor S (= cluster size) for `units` (sequence, KV head) pairs and

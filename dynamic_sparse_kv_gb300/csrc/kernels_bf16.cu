@@ -16,13 +16,8 @@ cudaError_t prepare_bf16() {
   return e != cudaSuccess ? e : prepare_all_modes<__nv_bfloat16, 128>();
 }
 
-int max_cluster_bf16(int head_dim) {
-  return head_dim == 64 ? max_cluster_size<__nv_bfloat16, 64>() : max_cluster_size<__nv_bfloat16, 128>();
-}
-
-int max_cluster_deep_bf16(int head_dim) {
-  return head_dim == 64 ? max_cluster_size<__nv_bfloat16, 64, kStagesDeep>()
-                        : max_cluster_size<__nv_bfloat16, 128, kStagesDeep>();
+int max_cluster_bf16(int head_dim, int variant) {
+  return head_dim == 64 ? max_cluster_of<__nv_bfloat16, 64>(variant) : max_cluster_of<__nv_bfloat16, 128>(variant);
 }
 
 int active_clusters_bf16(int head_dim, int cluster) {

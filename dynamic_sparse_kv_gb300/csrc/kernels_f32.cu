@@ -16,13 +16,8 @@ cudaError_t prepare_f32() {
   return e != cudaSuccess ? e : prepare_all_modes<float, 128>();
 }
 
-int max_cluster_f32(int head_dim) {
-  return head_dim == 64 ? max_cluster_size<float, 64>() : max_cluster_size<float, 128>();
-}
-
-int max_cluster_deep_f32(int head_dim) {
-  return head_dim == 64 ? max_cluster_size<float, 64, kStagesDeep>()
-                        : max_cluster_size<float, 128, kStagesDeep>();
+int max_cluster_f32(int head_dim, int variant) {
+  return head_dim == 64 ? max_cluster_of<float, 64>(variant) : max_cluster_of<float, 128>(variant);
 }
 
 // The selection kernel does not depend on the cache dtype; this unit hosts

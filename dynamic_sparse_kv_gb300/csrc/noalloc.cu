@@ -21,12 +21,10 @@ cudaError_t launch_bf16(int head_dim, int mode, const Params& p, cudaStream_t s)
 cudaError_t launch_f32(int head_dim, int mode, const Params& p, cudaStream_t s);
 cudaError_t prepare_bf16();
 cudaError_t prepare_f32();
-int max_cluster_bf16(int head_dim);
-int max_cluster_f32(int head_dim);
+int max_cluster_bf16(int head_dim, int variant);
+int max_cluster_f32(int head_dim, int variant);
 int active_clusters_bf16(int head_dim, int cluster);
 int active_clusters_f32(int head_dim, int cluster);
-int max_cluster_deep_bf16(int head_dim);
-int max_cluster_deep_f32(int head_dim);
 }  // namespace fastocr
 
 using namespace fastocr;
@@ -66,14 +64,14 @@ fastocr_status device_setup(int dev, DeviceState** out) {
     if (prepare_bf16() != cudaSuccess || prepare_f32() != cudaSuccess) return FASTOCR_ERR_CUDA;
     s.scratch = static_cast<float*>(ptr);
     s.num_sms = prop.multiProcessorCount;
-    s.max_cluster[FASTOCR_DTYPE_F32][0] = max_cluster_f32(64);
-    s.max_cluster[FASTOCR_DTYPE_F32][1] = max_cluster_f32(128);
-    s.max_cluster[FASTOCR_DTYPE_BF16][0] = max_cluster_bf16(64);
-    s.max_cluster[FASTOCR_DTYPE_BF16][1] = max_cluster_bf16(128);
-    s.max_cluster_deep[FASTOCR_DTYPE_F32][0] = max_cluster_deep_f32(64);
-    s.max_cluster_deep[FASTOCR_DTYPE_F32][1] = max_cluster_deep_f32(128);
-    s.max_cluster_deep[FASTOCR_DTYPE_BF16][0] = max_cluster_deep_bf16(64);
-    s.max_cluster_deep[FASTOCR_DTYPE_BF16][1] = max_cluster_deep_bf16(128);
+    s.max_cluster[FASTOCR_DTYPE_F32][0] = max_cluster_f32(64, kGeneral);
+    s.max_cluster[FASTOCR_DTYPE_F32][1] = max_cluster_f32(128, kGeneral);
+    s.max_cluster[FASTOCR_DTYPE_BF16][0] = max_cluster_bf16(64, kGeneral);
+    s.max_cluster[FASTOCR_DTYPE_BF16][1] = max_cluster_bf16(128, kGeneral);
+    s.max_cluster_deep[FASTOCR_DTYPE_F32][0] = max_cluster_f32(64, kDeep);
+    s.max_cluster_deep[FASTOCR_DTYPE_F32][1] = max_cluster_f32(128, kDeep);
+    s.max_cluster_deep[FASTOCR_DTYPE_BF16][0] = max_cluster_bf16(64, kDeep);
+    s.max_cluster_deep[FASTOCR_DTYPE_BF16][1] = max_cluster_bf16(128, kDeep);
     for (int dt = 0; dt < 2; ++dt)
       for (int wide = 0; wide < 2; ++wide)
         for (int c = 1; c <= s.max_cluster[dt][wide]; ++c)
@@ -166,7 +164,10 @@ extern "C" fastocr_status fastocr_focal_attend_noalloc(
                            st->max_cluster[d.dtype][wide], st->active[d.dtype][wide],
                            st->num_sms);
   p.pdl_early = (long)p.splits * p.Hkv * p.B <= st->num_sms;
-  p.deep = 2L * p.splits * p.Hkv * p.B <= st->num_sms && p.splits <= st->max_cluster_deep[d.dtype][wide];
+  p.variant = 2L * p.splits * p.Hkv * p.B <= st->num_sms &&
+                      p.splits <= st->max_cluster_deep[d.dtype][wide]
+                  ? kDeep
+                  : kGeneral;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const cudaError_t e = d.dtype == FASTOCR_DTYPE_BF16 ? launch_bf16(d.head_dim, kFocal, p, cs)
                                                       : launch_f32(d.head_dim, kFocal, p, cs);

@@ -99,7 +99,8 @@ class DecodeAttention:
 
     def __init__(self, k_cache, v_cache, block_table, *, q_heads: int, img_range=None,
                  max_img: int = 0, tau: float = 1.0, mode: str = "fastocr",
-                 rswa_prefix: int = 0, rswa_window: int = 0, splits=None, score_reduce=None):
+                 rswa_prefix: int = 0, rswa_window: int = 0, splits=None, variants=None,
+                 score_reduce=None):
         assert k_cache.is_cuda and k_cache.shape == v_cache.shape
         self.k_cache, self.v_cache = k_cache, v_cache
         self.layers, self.num_pages, self.kv_heads, self.page_size, self.head_dim = k_cache.shape
@@ -120,6 +121,9 @@ class DecodeAttention:
         if splits:
             for m, s in splits.items():
                 N.fastocr_set_splits(self.handle, m, s)
+        if variants:   # {mode slot: VARIANT_*}; tuning and tests only
+            for m, v in variants.items():
+                N.fastocr_set_variant(self.handle, m, v)
         self.seq_len = torch.zeros(self.batch, dtype=torch.int32, device=dev)
         self.kv = [N.make_kv(k_cache[l], v_cache[l], self.block_table, self.seq_len)
                    for l in range(self.layers)]

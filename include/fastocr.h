@@ -246,6 +246,14 @@ fastocr_status fastocr_set_splits(fastocr_handle* h, int32_t mode, int32_t split
 fastocr_status fastocr_read_probe(const void* src, int64_t bytes, uint32_t* sink,
                                   fastocr_stream stream);
 
+/* Override the kernel variant of a mode (0 = full/focal, 1 = sparse,
+ * 2 = R-SWA): 0 = automatic (default), 1 = general (6 warps of 2 stages, two
+ * CTAs an SM), 2 = deep (4 warps of 6 stages, one CTA an SM). Results do not
+ * depend on it (up to summation order); it exists for tuning and testing.
+ * Returns UNSUPPORTED for a variant whose shared memory does not fit this
+ * handle's dtype and head size. */
+fastocr_status fastocr_set_variant(fastocr_handle* h, int32_t mode, int32_t variant);
+
 /* Allocation-free focal layer. The pages describe no such call; it exists
  * for callers that may not allocate GPU memory at the point where they run
  * attention -- for example code living inside another framework's memory

@@ -222,8 +222,17 @@ def test_adaptive_reprofiling():
     assert not set(hist[1][1]) & set(first)
 
 
+VARIANTS = {"auto": None, "general": 1, "deep": 2}
+
+
+def _variants(name):
+    v = VARIANTS[name]
+    return None if v is None else {0: v, 1: v, 2: v}
+
+
+@pytest.mark.parametrize("variant", list(VARIANTS))
 @pytest.mark.parametrize("splits", [None, {0: 5, 1: 4, 2: 5}], ids=["auto", "forced"])
-def test_ragged_batch(splits):
+def test_ragged_batch(splits, variant):
     """One launch over sequences that differ in cache length, image position,
     image count (hence k) and R-SWA window position -- as in a continuously
     batched server: every sequence matches the oracle run on its own. Forced
@@ -238,7 +247,8 @@ def test_ragged_batch(splits):
     ranges = [(40, 320), (23, 300), (40, 250), (0, 320)]   # (start, N_img), inside [0, N_t)
     prefix, window = 100, 24
     dec = DecodeAttention(case.k_cache, case.v_cache, case.block_table, q_heads=wl.q_heads,
-                          img_range=case.img_range, max_img=wl.n_img, tau=wl.tau, splits=splits)
+                          img_range=case.img_range, max_img=wl.n_img, tau=wl.tau, splits=splits,
+                          variants=_variants(variant))
     dec.set_seq_len(n_max)                          # length hint: the longest sequence
     dec.set_seq_len(torch.tensor(n_ts, dtype=torch.int32, device="cuda"))
     img = torch.tensor(ranges, dtype=torch.int32, device="cuda")
@@ -270,8 +280,9 @@ def test_ragged_batch(splits):
     dec.close()
 
 
+@pytest.mark.parametrize("variant", list(VARIANTS))
 @pytest.mark.parametrize("splits", [None, {0: 16, 1: 16, 2: 16}], ids=["auto", "split16"])
-def test_degenerate_lengths(splits):
+def test_degenerate_lengths(splits, variant):
     """Edge cases in one launch: a cache of only the current token, an image
     range that is empty, starts at N_t, or holds the current token (which a
     gather layer then attends only if it was selected), and -- with 16
@@ -284,7 +295,8 @@ def test_degenerate_lengths(splits):
     ranges = [(0, 0), (0, 2), (16, 0), (1, 0), (5, 30), (0, 3)]
     prefix, window = 100, 24
     dec = DecodeAttention(case.k_cache, case.v_cache, case.block_table, q_heads=wl.q_heads,
-                          img_range=case.img_range, max_img=wl.n_img, tau=wl.tau, splits=splits)
+                          img_range=case.img_range, max_img=wl.n_img, tau=wl.tau, splits=splits,
+                          variants=_variants(variant))
     dec.set_seq_len(max(n_ts))
     dec.set_seq_len(torch.tensor(n_ts, dtype=torch.int32, device="cuda"))
     img = torch.tensor(ranges, dtype=torch.int32, device="cuda")
@@ -517,3 +529,49 @@ def test_score_reduce_path_whole_decode():
     run.run(0, case.wl.steps)
     compare_decode(run, case.wl.steps)
     assert len(calls) == 2 * (case.wl.steps - case.wl.warmup)   # two focal layers a step
+
+
+@pytest.mark.parametrize("variant", list(VARIANTS))
+def test_variants_long_lists(variant):
+    """Every kernel variant on lists longer than its row slice (several rounds
+    of staging) and on gather lists whose selection spans several tiles per
+    warp: full, focal, sparse and R-SWA outputs and the selection match the
+    oracle."""
+    from dynamic_sparse_kv_gb300 import DecodeAttention
+    from dynamic_sparse_kv_gb300 import _native as N
+    case = _case("qwen7b_b1", batch=2, layers=1, prompt=300, grid=(1, 40, 64), steps=900,
+                 tau=0.3)
+    wl = case.wl
+    t = 850
+    n_t = wl.seq_len_at(t)                          # 300 + 2560 + 851 tokens
+    prefix, window = 1500, 700
+    dec = DecodeAttention(case.k_cache, case.v_cache, case.block_table, q_heads=wl.q_heads,
+                          img_range=case.img_range, max_img=wl.n_img, tau=wl.tau,
+                          variants=_variants(variant))
+    dec.set_seq_len(n_t)
+    q = case.q_at(t)[0].contiguous()
+    out_full, out_focal, out_sparse, out_rswa = (torch.empty_like(q) for _ in range(4))
+    idx = torch.zeros(wl.batch, dec.stride, dtype=torch.int32, device="cuda")
+    k = torch.zeros(wl.batch, dtype=torch.int32, device="cuda")
+    N.fastocr_full_attend(dec.handle, q, dec.kv[0], out_full)
+    N.fastocr_focal_attend(dec.handle, q, dec.kv[0], case.img_range, wl.tau, out_focal, idx,
+                           dec.stride, k)
+    N.fastocr_sparse_attend(dec.handle, q, dec.kv[0], case.img_range, idx, dec.stride, k,
+                            out_sparse)
+    N.fastocr_rswa_attend(dec.handle, q, dec.kv[0], prefix, window, out_rswa)
+    torch.cuda.synchronize()
+    assert dec.device_status() == 0
+    kv = KVCache(case)
+    for b in range(wl.batch):
+        Kl, Vl = kv(0, b)
+        qb = np64(q[b])
+        assert_close(out_full[b], A.full_attend(qb, Kl, Vl, n_t), TOL["bf16"], f"full b={b}")
+        ref_out, ref_sel, sigma = A.focal_attend(qb, Kl, Vl, n_t, wl.prompt, wl.n_img, wl.tau)
+        assert_close(out_focal[b], ref_out, TOL["bf16"], f"focal b={b}")
+        got = idx[b, :int(k[b])].cpu().numpy()
+        check_selection(got, ref_sel, sigma, wl.prompt, f"focal b={b}")
+        assert_close(out_sparse[b], A.sparse_attend(qb, Kl, Vl, n_t, wl.prompt, wl.n_img, got),
+                     TOL["bf16"], f"sparse b={b}")
+        assert_close(out_rswa[b], A.rswa_attend(qb, Kl, Vl, n_t, prefix, window), TOL["bf16"],
+                     f"rswa b={b}")
+    dec.close()
