@@ -457,6 +457,7 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
     const int r = i * kRowsPerInst + row_lane;
     doff[i] = r * ROWB + ((ch_lane ^ (r & 7)) << 4);
   }
+  const uint64_t pol_stream = l2_policy_evict_first();   // K/V rows are read once
   auto issue = [&](int j, int n_round) {
     const int stage = j % ST;
     const int base = (warp + j * kWarps) * kTile;
@@ -475,8 +476,8 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
     for (int i = 0; i < kIss; ++i) {
       const size_t off = (size_t)max(rows[i], 0) * ROWB;
       const int bytes = rows[i] >= 0 ? 16 : 0;
-      cp_async16(sb + doff[i], kg_lane + off, bytes);
-      cp_async16(sb + doff[i] + kTile * ROWB, vg_lane + off, bytes);
+      cp_async16(sb + doff[i], kg_lane + off, bytes, pol_stream);
+      cp_async16(sb + doff[i] + kTile * ROWB, vg_lane + off, bytes, pol_stream);
     }
   };
 

@@ -105,10 +105,21 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
+// 16-byte asynchronous copy global -> shared (zero-filled past src_bytes),
+// with an L2 cache policy (from createpolicy).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes,
+                                               uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(dst),
+               "l"(src), "r"(src_bytes), "l"(pol)
                : "memory");
+}
+// L2 policy for data read once: its lines are the first to be evicted, so
+// the stream does not push out what is still to be read (a focal layer's
+// image logits, the next layer's prefetched rows).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
 }
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;\n" ::: "memory");
