@@ -30,5 +30,6 @@ def pytest_sessionfinish(session, exitstatus):
         return
     import json
     with open(path, "w") as f:
-        json.dump({k: {"max_abs_err": v[0], "max_abs_err_vs_rounded_oracle": v[1], "dtype": v[2]}
+        json.dump({k: {"max_abs_err": v[0], "max_abs_err_vs_rounded_oracle": v[1], "dtype": v[2],
+                       "max_err_in_output_ulps": v[3]}
                    for k, v in sorted(mod.ERRORS.items())}, f, indent=1)

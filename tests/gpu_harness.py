@@ -92,8 +92,15 @@ def assert_close(gpu: torch.Tensor, ref: np.ndarray, tol: float, where=""):
     assert err <= tol, f"{where}: max abs error {err:.3g} > {tol}"
     rounded = torch.from_numpy(np.ascontiguousarray(ref)).to(gpu.dtype).double().numpy()
     err_r = float(np.max(np.abs(got - rounded))) if ref.size else 0.0
-    rec = ERRORS.setdefault(_test_name(), [0.0, 0.0, str(gpu.dtype)])
-    rec[0], rec[1] = max(rec[0], float(err)), max(rec[1], err_r)
+    # error in units of the output format's spacing (bf16: 8 significant bits,
+    # fp32: 24) at the largest exact value of the same head's output row, i.e.
+    # relative to the scale of that output vector
+    bits = 8 if gpu.dtype == torch.bfloat16 else 24
+    scale = np.max(np.abs(ref), axis=-1, keepdims=True) if ref.size else ref
+    ulp = np.exp2(np.floor(np.log2(np.maximum(scale, 2.0 ** -30))) - (bits - 1))
+    n_ulp = float(np.max(np.abs(got - ref) / ulp)) if ref.size else 0.0
+    rec = ERRORS.setdefault(_test_name(), [0.0, 0.0, str(gpu.dtype), 0.0])
+    rec[0], rec[1], rec[3] = max(rec[0], float(err)), max(rec[1], err_r), max(rec[3], n_ulp)
     return float(err)
 
 
