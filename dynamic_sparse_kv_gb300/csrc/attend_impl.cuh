@@ -601,6 +601,7 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
       sm_.qf[ks][1] = have ? __ldcg(reinterpret_cast<const unsigned int*>(qrow + 16 * ks + 8 + 2 * tig)) : 0u;
     }
   }
+  bool relaid = false;   // the selection's rows were resolved again (CTA-uniform)
   if (MODE == kSparse) {
     // keep the speculative entries only if this CTA's share is unchanged
     const int k = __ldcg(p.k_in + b);
@@ -633,6 +634,7 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
       pre_issued = 0;
       n_sel_pad = (c.n_sel + kTile - 1) / kTile * kTile;
       resolve(0, n_txt_pad, min(n_txt_pad + n_sel_pad + c.has_cur, kSliceMax));
+      relaid = true;
     }
   }
   const int n_cta = n_txt_pad + n_sel_pad + c.has_cur;
@@ -662,7 +664,9 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
       for (int j = 0; j < D / 32; ++j) sf_.acc[h][j] = 0.f;
     }
   }
-  __syncthreads();
+  // the fp32 path's q and rows resolved again after the wait are read by
+  // every warp; otherwise each warp starts as soon as its own q has arrived
+  if (!kMma || relaid) __syncthreads();
 
   // lane constants of the ldmatrix addresses within a stage (bf16): K reads
   // row `lane & 15`, chunk 2ks + (lane >> 4); V reads row

@@ -575,3 +575,27 @@ def test_variants_long_lists(variant):
         assert_close(out_rswa[b], A.rswa_attend(qb, Kl, Vl, n_t, prefix, window), TOL["bf16"],
                      f"rswa b={b}")
     dec.close()
+
+
+@pytest.mark.parametrize("page", [1, 4, 64, 256])
+def test_page_sizes(page):
+    """Page sizes across the supported range (a power of two, 1..256 tokens):
+    the whole FastOCR schedule and an R-SWA pass match the oracle, so block
+    table lookups, slot arithmetic and pages that hold several kinds of tokens
+    are right at every size."""
+    case = _case("qwen7b_b1", batch=2, layers=3, prompt=21, grid=(1, 10, 17), steps=6,
+                 warmup=2, n_focal=1, tau=0.1, page_size=page)
+    run = GpuRun(case).run(0, case.wl.steps)
+    compare_decode(run, case.wl.steps)
+    wl = synth.workload("rswa_b16", batch=2, layers=1, rswa_prefix=70, prompt=70,
+                        rswa_window=9, steps=30, page_size=page)
+    rcase = synth.make_case(wl, device="cuda")
+    rrun = GpuRun(rcase).run(0, wl.steps, kind="rswa")
+    kv = KVCache(rcase)
+    for t in (0, 8, 9, 29):
+        n_t = wl.seq_len_at(t)
+        for b in range(wl.batch):
+            K, V = kv(0, b)
+            ref = A.rswa_attend(np64(rcase.q_at(t)[0, b]), K, V, n_t, wl.rswa_prefix,
+                                wl.rswa_window)
+            assert_close(rrun.outs[t][0, b], ref, TOL["bf16"], f"rswa page={page} t={t} b={b}")
