@@ -361,7 +361,6 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
   constexpr bool kMma = sizeof(T) == 2;
   constexpr int ROWB = SM::kRowBytes;
   constexpr int CH = ROWB / 16;                 // 16-byte chunks per row
-  constexpr int kElemPerChunk = 16 / (int)sizeof(T);
   const float kNegInf = -CUDART_INF_F;
 
   const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
@@ -565,7 +564,7 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
   }
   __syncthreads();
 #pragma unroll 1
-  for (int j = pre_issued; j < ST; ++j) {   // then the selection's (sparse)
+  for (int j = 0; j < ST; ++j) {
     const int end = (warp + j * kWarps + 1) * kTile;
     if (pre_issued == j && end <= n_pre) {
       issue(j, n_pre);

@@ -15,13 +15,14 @@
 // tiles of the slice independently through a cp.async pipeline (6 warps of 2
 // stages; 4 warps of 6 stages for grids that leave every CTA an SM of its
 // own), in 16-byte chunks into XOR-swizzled rows, so any gathered row is a
-// coalesced 256-byte read and ldmatrix is conflict-free. For bf16 the GQA group (g <= 8 query
+// coalesced 256-byte read and ldmatrix is conflict-free; the copies carry an
+// L2 evict-first policy (each row is read once). For bf16 the GQA group (g <= 8 query
 // heads) x 16 keys contraction and the P.V product run on the tensor cores
 // (mma.sync m16n8k16, keys / head dims on M, query heads on N); fp32 runs on
 // the CUDA cores. Softmax is online in the base-2 domain with a lazily moved
 // running max. The CTAs of a cluster push their partials into each other's
 // shared memory and merge after one cluster barrier (no global partials, no
-// spin-waits). In focal mode every CTA also stores its image tokens' logits
+// spin-waits); a single CTA merges its warps straight into the output. In focal mode every CTA also stores its image tokens' logits
 // and, after the merge, turns them into its KV head's share of the head-summed
 // probabilities; a separate one-CTA-per-sequence kernel, chained by
 // programmatic dependent launch, sums the KV heads and radix-selects the top
