@@ -73,8 +73,22 @@ def test_host_checks_without_gpu(lib):
                                   -1, None) == N.FASTOCR_ERR_NULL
     assert L.fastocr_profiler_select(None, 1, None, None, None) == N.FASTOCR_ERR_NULL
     assert L.fastocr_set_splits(None, 0, 1) == N.FASTOCR_ERR_NULL
+    assert L.fastocr_set_variant(None, 0, 1) == N.FASTOCR_ERR_NULL
     assert L.fastocr_set_length_hint(None, 100) == N.FASTOCR_ERR_NULL
+    assert L.fastocr_focal_scores(None, None, ctypes.byref(kv), None, None, None, 1,
+                                  None) == N.FASTOCR_ERR_NULL
+    assert L.fastocr_select(None, ctypes.byref(kv), None, None, 1, 0.5, None, 1, None,
+                            None) == N.FASTOCR_ERR_NULL
     assert L.fastocr_destroy(None) == N.FASTOCR_OK
+    # the read-only bandwidth probe checks its arguments before touching a GPU
+    buf = (ctypes.c_uint8 * 64)()
+    sink = ctypes.c_uint32()
+    addr = (ctypes.addressof(buf) + 15) // 16 * 16
+    assert L.fastocr_read_probe(None, 32, ctypes.byref(sink), None) == N.FASTOCR_ERR_NULL
+    assert L.fastocr_read_probe(addr, 32, None, None) == N.FASTOCR_ERR_NULL
+    for bad in (0, 8, 24, -16):
+        assert L.fastocr_read_probe(addr, bad, ctypes.byref(sink), None) == N.FASTOCR_ERR_INVALID
+    assert L.fastocr_read_probe(addr + 4, 32, ctypes.byref(sink), None) == N.FASTOCR_ERR_ALIGN
 
 
 def test_create_without_gpu_reports_no_device(lib):

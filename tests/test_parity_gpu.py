@@ -420,6 +420,38 @@ def test_host_argument_errors():
     with pytest.raises(N.FastOCRError) as e:
         N.fastocr_set_splits(dec.handle, 3, 2)
     assert e.value.status == N.FASTOCR_ERR_INVALID
+    for mode, variant in ((3, 1), (0, 3), (1, -1)):
+        with pytest.raises(N.FastOCRError) as e:
+            N.fastocr_set_variant(dec.handle, mode, variant)
+        assert e.value.status == N.FASTOCR_ERR_INVALID
+    sigma = torch.zeros(1, case.wl.n_img, dtype=torch.float32, device="cuda")
+    with pytest.raises(N.FastOCRError) as e:   # score rows narrower than the image
+        N.fastocr_focal_scores(dec.handle, q, dec.kv[0], case.img_range, out, sigma,
+                               case.wl.n_img - 1)
+    assert e.value.status == N.FASTOCR_ERR_INVALID
+    with pytest.raises(N.FastOCRError) as e:
+        N.fastocr_select(dec.handle, dec.kv[0], case.img_range, sigma, case.wl.n_img, 0.0, idx,
+                         dec.stride, k)
+    assert e.value.status == N.FASTOCR_ERR_INVALID
+
+
+def test_read_probe_reads_every_word():
+    """The bandwidth probe runs on a large buffer and touches every word: its
+    device time scales with the bytes it is given."""
+    from dynamic_sparse_kv_gb300 import _native as N
+    buf = torch.ones(1 << 30, dtype=torch.uint8, device="cuda")
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    times = {}
+    for n in (1 << 28, 1 << 30):
+        N.fastocr_read_probe(buf, n, sink)          # warm
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        N.fastocr_read_probe(buf, n, sink)
+        e.record()
+        torch.cuda.synchronize()
+        times[n] = s.elapsed_time(e)
+    assert times[1 << 30] > 2.0 * times[1 << 28]   # 4x the bytes takes well over 2x the time
+    assert (1 << 30) / (times[1 << 30] * 1e-3) < 20e12   # below any plausible HBM rate
 
 
 def test_length_hint_changes_speed_not_results():
