@@ -69,6 +69,8 @@ def _load() -> ctypes.CDLL:
         "fastocr_rswa_attend": ([P, P, ctypes.POINTER(fastocr_kv), I32, I32, P, P], I32),
         "fastocr_profiler_reset": ([P, P], I32),
         "fastocr_profiler_select": ([P, I32, ctypes.POINTER(I32), ctypes.POINTER(F64), P], I32),
+        "fastocr_profiler_read": ([P, ctypes.POINTER(F64), P], I32),
+        "fastocr_profiler_load": ([P, ctypes.POINTER(F64), P], I32),
         "fastocr_device_status": ([P, ctypes.POINTER(I32), P], I32),
         "fastocr_set_splits": ([P, I32, I32], I32),
         "fastocr_set_variant": ([P, I32, I32], I32),
@@ -188,6 +190,19 @@ def fastocr_profiler_select(handle, n_focal, num_layers, stream=None):
     _check("fastocr_profiler_select",
            lib.fastocr_profiler_select(handle, int(n_focal), layers, ratio, _stream(stream)))
     return tuple(int(x) for x in layers), [float(x) for x in ratio]
+
+
+def fastocr_profiler_read(handle, num_layers, stream=None) -> list:
+    """The accumulated image mass of every layer (synchronises the stream)."""
+    mass = (ctypes.c_double * num_layers)()
+    _check("fastocr_profiler_read", lib.fastocr_profiler_read(handle, mass, _stream(stream)))
+    return [float(x) for x in mass]
+
+
+def fastocr_profiler_load(handle, mass, stream=None) -> None:
+    """Load the accumulated image mass of every layer (len(mass) = num_layers)."""
+    arr = (ctypes.c_double * len(mass))(*[float(x) for x in mass])
+    _check("fastocr_profiler_load", lib.fastocr_profiler_load(handle, arr, _stream(stream)))
 
 
 def fastocr_device_status(handle, stream=None) -> int:

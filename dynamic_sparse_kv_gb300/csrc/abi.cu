@@ -375,6 +375,28 @@ fastocr_status fastocr_profiler_select(fastocr_handle* h, int32_t n_focal, int32
   return FASTOCR_OK;
 }
 
+fastocr_status fastocr_profiler_read(fastocr_handle* h, double* mass_out, fastocr_stream stream) {
+  if (!h || !mass_out) return FASTOCR_ERR_NULL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(mass_out, h->profile, (size_t)h->dims.num_layers * sizeof(double),
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return FASTOCR_ERR_CUDA;
+  return FASTOCR_OK;
+}
+
+fastocr_status fastocr_profiler_load(fastocr_handle* h, const double* mass_in,
+                                     fastocr_stream stream) {
+  if (!h || !mass_in) return FASTOCR_ERR_NULL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // synchronous on the stream: the caller's host array may go away on return
+  if (cudaMemcpyAsync(h->profile, mass_in, (size_t)h->dims.num_layers * sizeof(double),
+                      cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return FASTOCR_ERR_CUDA;
+  return FASTOCR_OK;
+}
+
 fastocr_status fastocr_device_status(fastocr_handle* h, int32_t* status, fastocr_stream stream) {
   if (!h || !status) return FASTOCR_ERR_NULL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -318,30 +318,37 @@ constexpr bool variant_fits() {
 
 // Split-K factor S (= cluster size) for `units` (sequence, KV head) pairs and
 // attend lists of about `len` tokens; active[s] = clusters of s CTAs the
-// device holds at once, num_sms its SM count. Model: a CTA streams its share
-// of len/S tokens at ~8 ns per token when it runs alone, slowed down when a
-// wave of CTAs together asks for more than HBM delivers (~40 GB/s per CTA
-// under load); clusters run in waves of active[S]; every doubling of the
-// cluster adds ~0.25 us of merge and barrier latency; a grid of at most
-// num_sms CTAs also lets the next kernel's CTAs stage their first tiles
-// while it runs (programmatic dependent launch), worth ~1.5 us. Fitted to
-// graph-replayed decode steps on GB300 (1 sequence: ~6 splits for gather
-// layers, 16 for full ones; 32 sequences: 1 and 2; 8 sequences of 16k
-// image tokens: 4 for gather layers).
+// device holds at once, num_sms its SM count. Model: clusters run in waves of
+// active[S]; a wave costs a fixed ~4 us (CTA start, pipeline fill, merge and
+// cluster barrier) plus its CTAs' share of len/S tokens at ~8 ns per token,
+// slowed down when the wave's CTAs together ask for more than HBM delivers
+// (~30 GB/s per CTA under load); a partial last wave is charged for the CTAs
+// it holds. Every doubling of the cluster adds ~0.25 us of merge latency; a
+// grid of at most num_sms CTAs also lets the next kernel's CTAs stage their
+// first tiles while it runs (programmatic dependent launch), worth ~3 us.
+// Fitted to forced split counts of every layer kind on GB300 (graph-replayed
+// layers, L2 flushed; 4 to 640 units of 525 to 18.5k tokens): the choice is
+// within 3% of the fastest forced count on each (1 sequence: 16 splits for
+// full layers, 12 for gather ones; 32 sequences: 2 and 1; 80 or more
+// sequences: 1 for gather layers).
 inline int choose_splits(long units, long len, int max_splits, const int* active, int num_sms) {
-  const double ns_per_token = 8.0, cta_gbs = 40.0, hbm_gbs = 6500.0, us_per_doubling = 0.25,
-               overlap_us = 1.5;
+  const double ns_per_token = 8.0, cta_gbs = 30.0, hbm_gbs = 6500.0, wave_fixed_us = 4.0,
+               us_per_doubling = 0.25, overlap_us = 3.0;
   if (len < 1) len = 1;
   int best = 1;
   double best_cost = 1e300;
   for (int s = 1; s <= max_splits; ++s) {
     const int act = active[s];
     if (act < 1) continue;
-    const long waves = (units + act - 1) / act;
-    const long ctas_in_wave = (units < act ? units : (long)act) * s;
-    const double slow = ctas_in_wave * cta_gbs / hbm_gbs > 1.0 ? ctas_in_wave * cta_gbs / hbm_gbs : 1.0;
-    const double per_cta_us = ((len + s - 1) / s) * ns_per_token * 1e-3 * slow;
-    double cost = waves * per_cta_us + us_per_doubling * log2((double)s);
+    const double chunk_us = ((len + s - 1) / s) * ns_per_token * 1e-3;
+    // one wave of `clusters` clusters
+    auto wave_us = [&](long clusters) {
+      const double load = (double)clusters * s * cta_gbs / hbm_gbs;
+      return wave_fixed_us + chunk_us * (load > 1.0 ? load : 1.0);
+    };
+    const long full = units / act, rest = units % act;
+    double cost = full * wave_us(act) + (rest ? wave_us(rest) : 0.0) +
+                  us_per_doubling * log2((double)s);
     if (units * s <= num_sms) cost -= overlap_us;
     if (cost < best_cost - 1e-9) {
       best_cost = cost;

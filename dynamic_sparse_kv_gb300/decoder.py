@@ -213,6 +213,50 @@ class DecodeAttention:
             return self.finish_warmup(n_focal, stream)[0]
         return None
 
+    # ------------------------------------------------------------ checkpoint
+    def state_dict(self, stream=None) -> dict:
+        """The method's state between decode steps, on the host: the focal set
+        C, the selections of the focal layers (the deepest one is F_last, the
+        next step's carried selection) and, while a warm-up window is open, its
+        per-layer selections and the profiler's accumulated image mass.
+        Synchronises the stream. The KV cache is the caller's and not part of it."""
+        if stream is not None:
+            stream.synchronize()
+        else:
+            torch.cuda.synchronize(self.k_cache.device)
+        st = {"batch": self.batch, "layers": self.layers, "stride": self.stride,
+              "tau": self.tau, "max_img": self.max_img, "focal": tuple(self.focal),
+              "has_f_last": self.has_f_last,
+              "sel": {l: (idx.cpu(), k.cpu()) for l, (idx, k) in self.sel.items()},
+              "warm": None}
+        if self.warm_idx is not None:
+            st["warm"] = (self.warm_idx.cpu(), self.warm_k.cpu(),
+                          N.fastocr_profiler_read(self.handle, self.layers, stream))
+        return st
+
+    def load_state_dict(self, st: dict, stream=None) -> None:
+        """Resume from state_dict() of a decoder over the same shapes and tau."""
+        for key in ("batch", "layers", "stride", "tau", "max_img"):
+            if st[key] != getattr(self, key):
+                raise ValueError(f"checkpoint {key}={st[key]!r}, decoder has {getattr(self, key)!r}")
+        if st["focal"]:
+            self.set_focal_layers(st["focal"])
+        else:
+            self.focal, self.sel = (), {}
+        for l, (idx, k) in st["sel"].items():
+            self.sel[l][0].copy_(idx)
+            self.sel[l][1].copy_(k)
+        self.has_f_last = bool(st["has_f_last"])
+        if st["warm"] is None:
+            self.warm_idx = self.warm_k = None
+        else:
+            warm_idx, warm_k, mass = st["warm"]
+            dev = self.k_cache.device
+            self.warm_idx = warm_idx.to(dev).contiguous()
+            self.warm_k = warm_k.to(dev).contiguous()
+            N.fastocr_profiler_load(self.handle, mass, stream)
+        torch.cuda.synchronize(self.k_cache.device)
+
     # ------------------------------------------------------------ steps
     def focal_layer(self, l, q_l, out_l, idx, k, stream=None):
         """One focal layer: attention, image scores and the top-k selection."""

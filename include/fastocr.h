@@ -217,6 +217,16 @@ fastocr_status fastocr_profiler_reset(fastocr_handle* h, fastocr_stream stream);
 fastocr_status fastocr_profiler_select(fastocr_handle* h, int32_t n_focal, int32_t* layers_out,
                                        double* ratio_out, fastocr_stream stream);
 
+/* Checkpoint and resume of the warm-up profile [FGP]: copy the accumulated
+ * image-attention mass of every layer to mass_out (host, num_layers doubles;
+ * synchronises `stream`), or load it from mass_in (host, num_layers doubles;
+ * the copy is complete when the call returns). Together with the focal set C
+ * and the F_last selection, which the caller owns, this is the whole state
+ * the method carries between decode steps. */
+fastocr_status fastocr_profiler_read(fastocr_handle* h, double* mass_out, fastocr_stream stream);
+fastocr_status fastocr_profiler_load(fastocr_handle* h, const double* mass_in,
+                                     fastocr_stream stream);
+
 /* Read the device status word (FASTOCR_DEV_* bits, 0 = clean) into *status
  * (host) and clear it. Synchronises `stream`. */
 fastocr_status fastocr_device_status(fastocr_handle* h, int32_t* status, fastocr_stream stream);

@@ -10,8 +10,9 @@ import pytest
 import oracle.attention as A
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-# a GB300-like table of co-resident clusters per size (2 CTAs per SM, 152 SMs)
-ACTIVE = [304, 152, 101, 76, 60, 50, 43, 38, 33, 30, 27, 25, 23, 21, 20, 19]
+# co-resident clusters of 1..16 CTAs of the general variant on a GB300
+# (152 SMs, 2 CTAs per SM), as the occupancy query reports them
+ACTIVE = [304, 152, 97, 74, 58, 46, 38, 36, 30, 28, 23, 23, 19, 14, 14, 14]
 
 
 @pytest.fixture(scope="module")
@@ -67,9 +68,28 @@ def test_split_choice_grows_with_length(probe):
 
 
 def test_split_choice_on_the_fitted_shapes(probe):
-    # (sequence, KV head) units and attend lengths of the benchmarked layers
-    got = _splits(probe, [(4, 4417, 16, ACTIVE),     # batch 1, full / focal layer
-                          (128, 8449, 16, ACTIVE),   # 32 sequences, focal layer
-                          (128, 667, 16, ACTIVE),    # 32 sequences, gather layer
-                          (1, 1, 16, ACTIVE)])       # one token: nothing to split
-    assert got == [16, 2, 1, 1]
+    # (sequence, KV head) units and attend lengths of layers whose split count
+    # was swept on a GB300; each expected value is within 3% of the fastest
+    # forced count there
+    rows = [((4, 4417), 16),      # batch 1, full / focal layer
+            ((4, 525), 12),       # batch 1, gather layer
+            ((32, 18496), 7),     # 8 sequences of 16k image tokens, focal layer
+            ((32, 2932), 4),      # ... gather layer
+            ((128, 8449), 2),     # 32 sequences, focal layer
+            ((128, 667), 1),      # 32 sequences, gather layer
+            ((320, 666), 1),      # 80 sequences, gather layer: one split, not six
+            ((512, 8448), 1),     # 128 sequences, focal layer
+            ((512, 666), 1),      # 128 sequences, gather layer
+            ((640, 666), 1),      # 160 sequences, gather layer
+            ((320, 2752), 3),     # R-SWA, 32 sequences x 10 heads
+            ((480, 2752), 1),     # R-SWA, 48 sequences
+            ((1, 1), 1)]          # one token: nothing to split
+    got = _splits(probe, [(u, n, 16, ACTIVE) for (u, n), _ in rows])
+    assert got == [want for _, want in rows]
+
+
+def test_split_choice_one_split_when_one_split_fills_the_device(probe):
+    """Short gather lists over more units than the device holds CTAs: extra
+    splits only add waves of fixed CTA cost."""
+    rows = [(u, n, 16, ACTIVE) for u in (304, 400, 608, 1024, 4096) for n in (300, 700)]
+    assert _splits(probe, rows) == [1] * len(rows)

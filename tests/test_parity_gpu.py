@@ -222,6 +222,44 @@ def test_adaptive_reprofiling():
     assert not set(hist[1][1]) & set(first)
 
 
+def test_checkpoint_resume():
+    """The method's state saved mid-warm-up and again in the steady decode and
+    loaded into fresh decoders: the resumed decode gives the same outputs and
+    selections as the uninterrupted one, bit for bit, and both match the
+    oracle. The profiler's mass, the warm-up selections, C and F_last are what
+    carry over."""
+    case = _case("qwen7b_b1", batch=2, layers=5, prompt=24, grid=(1, 12, 16), steps=14,
+                 warmup=4, n_focal=2, tau=0.1)
+    wl = case.wl
+    whole = GpuRun(case).run(0, wl.steps)
+    t1, t2 = 2, 9                                  # inside the warm-up; steady decode
+    part = GpuRun(case).run(0, t1)
+    st = part.dec.state_dict()
+    assert st["warm"] is not None and st["focal"] == ()
+    assert len(st["warm"][2]) == wl.layers and all(m > 0 for m in st["warm"][2])
+    part.dec.close()
+    res = GpuRun(case)
+    res.dec.load_state_dict(st)
+    res.run(t1, t2)
+    st2 = res.dec.state_dict()
+    assert st2["focal"] == whole.focal and st2["has_f_last"]
+    res.dec.close()
+    res2 = GpuRun(case)
+    res2.dec.load_state_dict(st2)
+    res2.focal = tuple(st2["focal"])
+    res2.run(t2, wl.steps)
+    for t in range(wl.steps):
+        got = (part if t < t1 else res if t < t2 else res2)
+        assert torch.equal(got.outs[t], whole.outs[t]), f"step {t}"
+        for l, sel in whole.sels[t].items():
+            for b in range(wl.batch):
+                assert np.array_equal(got.sels[t][l][b], sel[b]), f"step {t} layer {l} seq {b}"
+    compare_decode(whole, wl.steps)
+    with pytest.raises(ValueError):
+        bad = GpuRun(case, tau=0.2)
+        bad.dec.load_state_dict(st2)
+
+
 VARIANTS = {"auto": None, "general": 1, "deep": 2}
 
 
