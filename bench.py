@@ -429,24 +429,31 @@ class Bench:
         med = statistics.median(passes)
         return reduce_max(med, self.world, self.dev), passes, wall, clocks
 
-    def time_replays(self, dec, cap, n):
-        """Median µs of n replays of cap (steps staged as in the timed pass, L2
-        flushed before each), and the staged decode steps."""
+    def time_replays(self, dec, cap, reps=2):
+        """µs of one replay of cap averaged over the decode steps of the timed
+        pass (the same K steps, staged the same way, L2 flushed before each):
+        each step's time is the median of `reps` replays, and the result is
+        their mean, so it is comparable with the step time. Also returns the
+        staged decode steps."""
         torch = self.torch
-        W = self.args.warmup
-        ts, steps = [], []
-        for i in range(W + n):
+        K, W = self.args.steps, self.args.warmup
+        for i in range(W):
             self.stage(dec, cap, i)
             self.flush.zero_()
-            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s.record()
             cap.replay()
-            e.record()
-            torch.cuda.synchronize()
-            if i >= W:
-                ts.append(s.elapsed_time(e) * 1e3)
-                steps.append(self.t_of(i))
-        return reduce_max(statistics.median(ts), self.world, self.dev), steps
+        per_step = [[] for _ in range(K)]
+        for _ in range(reps):
+            for j in range(K):
+                self.stage(dec, cap, W + j)
+                self.flush.zero_()
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record()
+                cap.replay()
+                e.record()
+                torch.cuda.synchronize()
+                per_step[j].append(s.elapsed_time(e) * 1e3)
+        us = statistics.fmean(statistics.median(x) for x in per_step)
+        return reduce_max(us, self.world, self.dev), [self.t_of(W + j) for j in range(K)]
 
     # ---- per-kind graphs: the step's layers of one kind, in step order
     def kind_fns(self, dec):
@@ -501,13 +508,13 @@ class Bench:
                                         out[first_sparse], stream)
         return fn
 
-    def kernel_breakdown(self, dec, us_per_step, n_rep):
+    def kernel_breakdown(self, dec, us_per_step):
         from dynamic_sparse_kv_gb300 import CapturedStep
         wl = self.wl
         kernels, alone = {}, {}
         for kind, (fn, layers, launches) in self.kind_fns(dec).items():
             cap = CapturedStep(dec, kind, fn=fn, launches=launches)
-            us, steps = self.time_replays(dec, cap, n_rep)
+            us, steps = self.time_replays(dec, cap)
             del cap
             k_seq = dec.sel[max(dec.focal)][1].tolist() if self.kind == "fastocr" else None
             bpl = statistics.fmean(kv_bytes(wl, kind, wl.seq_len_at(t), k_seq) for t in steps)
@@ -517,7 +524,7 @@ class Bench:
                              "share": us / us_per_step}
             cap1 = CapturedStep(dec, kind + "_alone", fn=self.single_fn(dec, kind),
                                 launches=launches // layers)
-            us1, steps1 = self.time_replays(dec, cap1, n_rep)
+            us1, steps1 = self.time_replays(dec, cap1)
             del cap1
             b1 = statistics.fmean(kv_bytes(wl, kind, wl.seq_len_at(t), k_seq) for t in steps1)
             alone[kind] = {"us": us1, "kv_bytes": b1, "gbs": b1 / (us1 * 1e-6) / 1e9}
@@ -622,8 +629,7 @@ def run_workload(args, name, rank, world, dev, flush, *, headline, sampler_gpu=N
     status = dec.device_status()
     assert status == 0, f"device status {status}"
     us_per_step = ms_pass * 1e3 / K
-    n_rep = 30
-    kernels, alone = bn.kernel_breakdown(dec, us_per_step, n_rep)
+    kernels, alone = bn.kernel_breakdown(dec, us_per_step)
     check = kinds_check(kernels, us_per_step)
     e2e = None if args.no_e2e else bn.e2e(dec, cap)
     compare = {}
