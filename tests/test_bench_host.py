@@ -81,3 +81,37 @@ def test_reference_arm_echoes_steps_and_config(monkeypatch):
     assert r["config"]["workload"] == args.workload == "serving_b32"
     assert r["config"]["tau"] == synth.workload("serving_b32").tau
     assert r["config"]["batch_per_gpu"] == 32
+
+
+def test_per_kind_timings_see_the_timed_pass_steps():
+    """The per-kind graphs are replayed on exactly the decode steps of the
+    timed pass (each step the same number of times), so their times add up
+    to the step time for workloads whose lists grow along the decode."""
+    import types
+
+    class Ev:
+        def record(self):
+            pass
+
+        def elapsed_time(self, other):
+            return 1.0
+
+    fake_torch = types.SimpleNamespace(cuda=types.SimpleNamespace(
+        Event=lambda enable_timing=True: Ev(), synchronize=lambda *a: None))
+    bn = object.__new__(bench.Bench)
+    bn.torch = fake_torch
+    bn.args = bench.parse_args(["--steps", "12", "--warmup", "3"])
+    bn.world, bn.dev = 1, None
+    bn.flush = types.SimpleNamespace(zero_=lambda: None)
+    bn.wl = synth.workload("multipage_b8")
+    bn.t0_steady, bn.span = bn.wl.warmup, bn.wl.steps - bn.wl.warmup
+    staged = []
+    bn.stage = lambda dec, cap, i: staged.append(bn.t_of(i))
+    cap = types.SimpleNamespace(replay=lambda: None)
+    K, W = 12, 3
+    us, steps = bn.time_replays(None, cap, reps=2)
+    timed = [bn.t_of(W + j) for j in range(K)]
+    assert steps == timed
+    assert sorted(staged[W:]) == sorted(timed * 2)
+    assert len(set(timed)) == K and max(timed) - min(timed) > bn.span // 2   # the whole decode
+    assert us == 1000.0
