@@ -586,6 +586,53 @@ def test_head_sharded_focal():
     assert dec.device_status() == 0
 
 
+@pytest.mark.parametrize("max_img", [300, 2048, 2049, 5000, 8192, 16384])
+@pytest.mark.parametrize("pattern", ["few_values", "constant", "distinct"])
+def test_select_kernel_exact(max_img, pattern):
+    """The selection kernel alone (fastocr_select on caller scores) against the
+    oracle's top-k, exactly: image ranges of 1 to 16384 tokens, so the
+    sequence's keys are spread over 1 to 8 CTAs of a cluster; ragged sizes in
+    one launch; scores with many ties (a handful of values, or all equal),
+    so the k-th score's tie group crosses CTA boundaries and the lowest
+    positions must win."""
+    from dynamic_sparse_kv_gb300 import _native as N
+    B, page = 3, 16
+    sizes = [max_img, max(1, max_img - 37), max(1, max_img // 3)]
+    starts = [5, 0, 17]
+    n_t = max(s + n for s, n in zip(starts, sizes)) + 9
+    pages = -(-n_t // page)
+    h = N.fastocr_create(B, 4, 2, 64, N.FASTOCR_DTYPE_BF16, page, pages, max_img, 1)
+    kc = torch.zeros(B * pages, 2, page, 64, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    bt = torch.arange(B * pages, dtype=torch.int32, device="cuda").view(B, pages)
+    seq_len = torch.full((B,), n_t, dtype=torch.int32, device="cuda")
+    kv = N.make_kv(kc, vc, bt, seq_len)
+    img = torch.tensor(list(zip(starts, sizes)), dtype=torch.int32, device="cuda")
+    g = torch.Generator().manual_seed(max_img * 7 + len(pattern))
+    if pattern == "few_values":
+        sig = torch.randint(0, 5, (B, max_img), generator=g).float() * 0.25
+    elif pattern == "constant":
+        sig = torch.full((B, max_img), 0.5)
+    else:
+        sig = torch.rand(B, max_img, generator=g)
+    for tau in (0.05, 0.5):
+        stride = A.keep_count(tau, max_img)
+        idx = torch.full((B, stride), -1, dtype=torch.int32, device="cuda")
+        k = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+        N.fastocr_select(h, kv, img, sig.cuda(), max_img, tau, idx, stride, k)
+        torch.cuda.synchronize()
+        for b in range(B):
+            n = sizes[b]
+            kk = A.keep_count(tau, n)
+            assert int(k[b]) == kk
+            want = starts[b] + A.select_top(sig[b, :n].double().numpy(), kk)
+            got = idx[b, :kk].cpu().numpy()
+            assert np.array_equal(got, want), (max_img, pattern, tau, b)
+            assert (idx[b, kk:] == -1).all()
+    assert N.fastocr_device_status(h) == 0
+    N.fastocr_destroy(h)
+
+
 def test_score_reduce_path_whole_decode():
     """DecodeAttention with a score_reduce hook (one shard: the hook adds
     nothing) runs its focal layers as scores -> reduce -> select; the whole
