@@ -66,6 +66,8 @@ def _load() -> ctypes.CDLL:
         "fastocr_focal_scores": ([P, P, ctypes.POINTER(fastocr_kv), P, P, P, I32, P], I32),
         "fastocr_select": ([P, ctypes.POINTER(fastocr_kv), P, P, I32, F64, P, I32, P, P], I32),
         "fastocr_sparse_attend": ([P, P, ctypes.POINTER(fastocr_kv), P, P, I32, P, P, P], I32),
+        "fastocr_sparse_attend_ex": ([P, P, ctypes.POINTER(fastocr_kv), P, P, I32, P, P,
+                                      ctypes.c_uint32, P], I32),
         "fastocr_rswa_attend": ([P, P, ctypes.POINTER(fastocr_kv), I32, I32, P, P], I32),
         "fastocr_profiler_reset": ([P, P], I32),
         "fastocr_profiler_select": ([P, I32, ctypes.POINTER(I32), ctypes.POINTER(F64), P], I32),
@@ -171,6 +173,19 @@ def fastocr_sparse_attend(handle, q, kv: fastocr_kv, img_range, idx, idx_stride,
            lib.fastocr_sparse_attend(handle, _ptr(q), ctypes.byref(kv), _ptr(img_range),
                                      _ptr(idx), int(idx_stride), _ptr(k), _ptr(out),
                                      _stream(stream)))
+
+
+SELECTION_FINAL = 1   # FASTOCR_SELECTION_FINAL
+
+
+def fastocr_sparse_attend_ex(handle, q, kv: fastocr_kv, img_range, idx, idx_stride, k, out,
+                             flags: int, stream=None) -> None:
+    """fastocr_sparse_attend with flags; SELECTION_FINAL: idx and k were written
+    before the kernel preceding this call on the stream began."""
+    _check("fastocr_sparse_attend_ex",
+           lib.fastocr_sparse_attend_ex(handle, _ptr(q), ctypes.byref(kv), _ptr(img_range),
+                                        _ptr(idx), int(idx_stride), _ptr(k), _ptr(out),
+                                        int(flags), _stream(stream)))
 
 
 def fastocr_rswa_attend(handle, q, kv: fastocr_kv, prefix_len, window, out, stream=None) -> None:

@@ -312,23 +312,31 @@ fastocr_status fastocr_select(fastocr_handle* h, const fastocr_kv* kv, const int
                                                                             : FASTOCR_ERR_CUDA;
 }
 
-fastocr_status fastocr_sparse_attend(fastocr_handle* h, const void* q, const fastocr_kv* kv,
-                                     const int32_t* img_range, const int32_t* idx,
-                                     int32_t idx_stride, const int32_t* k, void* out,
-                                     fastocr_stream stream) {
+fastocr_status fastocr_sparse_attend_ex(fastocr_handle* h, const void* q, const fastocr_kv* kv,
+                                        const int32_t* img_range, const int32_t* idx,
+                                        int32_t idx_stride, const int32_t* k, void* out,
+                                        uint32_t flags, fastocr_stream stream) {
   if (!h || !q || !out || !img_range || !idx || !k) return FASTOCR_ERR_NULL;
   fastocr_status st = check_kv(h, kv);
   if (st != FASTOCR_OK) return st;
   if (!aligned16(q) || !aligned16(out)) return FASTOCR_ERR_ALIGN;
-  if (idx_stride < 1) return FASTOCR_ERR_INVALID;
+  if (idx_stride < 1 || (flags & ~(uint32_t)FASTOCR_SELECTION_FINAL)) return FASTOCR_ERR_INVALID;
   Params p = base_params(h, q, kv, out);
   p.img_range = img_range;
   p.idx = idx;
   p.idx_stride = idx_stride;
   p.k_in = k;
+  p.sel_final = (flags & FASTOCR_SELECTION_FINAL) ? 1 : 0;
   // text tokens (cache minus the image) plus at most idx_stride selected ones
   const long text = std::max(0L, expected_tokens(h) - (long)h->dims.max_img_tokens);
   return launch(h, kSparse, std::min(expected_tokens(h), text + idx_stride), p, stream);
+}
+
+fastocr_status fastocr_sparse_attend(fastocr_handle* h, const void* q, const fastocr_kv* kv,
+                                     const int32_t* img_range, const int32_t* idx,
+                                     int32_t idx_stride, const int32_t* k, void* out,
+                                     fastocr_stream stream) {
+  return fastocr_sparse_attend_ex(h, q, kv, img_range, idx, idx_stride, k, out, 0u, stream);
 }
 
 fastocr_status fastocr_rswa_attend(fastocr_handle* h, const void* q, const fastocr_kv* kv,

@@ -601,7 +601,22 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
     }
   }
   bool relaid = false;   // the selection's rows were resolved again (CTA-uniform)
-  if (MODE == kSparse) {
+  if (MODE == kSparse && p.sel_final) {
+    // the caller guarantees that k and idx were written before the previous
+    // kernel began, so the reading before the wait is the real selection:
+    // only report its faulty entries (each thread its own, no barrier)
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int u = n_txt_pad + tid + j * kThreads;
+      if (u >= spec_u1) continue;
+      if (spec_raw[j] < c.img_start || spec_raw[j] >= c.img_start + c.n_img)
+        bad |= kDevBadSelection;
+      else if (spos[u] < 0)
+        bad |= kDevBadPage;
+    }
+    const int k_read = *reinterpret_cast<const int*>(smem + SM::kSpecK);   // clamped before use
+    if (tid == 0 && (k_read < 0 || k_read > min(c.n_img, p.idx_stride))) bad |= kDevBadSelection;
+  } else if (MODE == kSparse) {
     // keep the speculative entries only if this CTA's share is unchanged
     const int k = __ldcg(p.k_in + b);
     int raw2[kPer];

@@ -75,6 +75,7 @@ struct Params {
   const int32_t* idx;        // sparse: selected positions
   int idx_stride;
   const int32_t* k_in;       // sparse: [B]
+  int sel_final;             // sparse: idx and k_in were final before the previous kernel began
   int32_t* idx_out;          // focal: [B, idx_stride]
   int32_t* k_out;            // focal: [B]
   double tau;

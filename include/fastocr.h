@@ -199,6 +199,22 @@ fastocr_status fastocr_sparse_attend(fastocr_handle* h, const void* q, const fas
                                      int32_t idx_stride, const int32_t* k, void* out,
                                      fastocr_stream stream);
 
+/* fastocr_sparse_attend with flags (0 = the call above). FASTOCR_SELECTION_FINAL:
+ * the caller guarantees that idx and k were written before the kernel
+ * preceding this call on `stream` began (e.g. a gather layer that is not the
+ * first after the focal layer whose selection it uses: the selection kernel
+ * is then two or more launches back, and programmatic dependent launch lets
+ * a kernel start only once the one before its predecessor has completed).
+ * The kernel then takes the selection it reads before the wait as final and
+ * skips re-reading it after the wait (and the CTA barrier that check needs).
+ * With the flag set and the guarantee broken, the layer may attend a stale
+ * selection; nothing faults. Other flag bits: FASTOCR_ERR_INVALID. */
+#define FASTOCR_SELECTION_FINAL 1u
+fastocr_status fastocr_sparse_attend_ex(fastocr_handle* h, const void* q, const fastocr_kv* kv,
+                                        const int32_t* img_range, const int32_t* idx,
+                                        int32_t idx_stride, const int32_t* k, void* out,
+                                        uint32_t flags, fastocr_stream stream);
+
 /* R-SWA layer [RSWA]: attention over [0, prefix_len) and the last `window`
  * tokens of [prefix_len, N_t), the current token included. prefix_len >= 0,
  * window >= 0. */

@@ -68,6 +68,8 @@ def test_host_checks_without_gpu(lib):
     assert L.fastocr_full_attend(None, None, ctypes.byref(kv), None, None) == N.FASTOCR_ERR_NULL
     assert L.fastocr_sparse_attend(None, None, ctypes.byref(kv), None, None, 1, None, None,
                                    None) == N.FASTOCR_ERR_NULL
+    assert L.fastocr_sparse_attend_ex(None, None, ctypes.byref(kv), None, None, 1, None, None,
+                                      N.SELECTION_FINAL, None) == N.FASTOCR_ERR_NULL
     assert L.fastocr_rswa_attend(None, None, ctypes.byref(kv), 0, 0, None, None) == N.FASTOCR_ERR_NULL
     assert L.fastocr_focal_attend(None, None, ctypes.byref(kv), None, 0.5, None, None, 1, None,
                                   -1, None) == N.FASTOCR_ERR_NULL

@@ -471,6 +471,57 @@ def test_host_argument_errors():
         N.fastocr_select(dec.handle, dec.kv[0], case.img_range, sigma, case.wl.n_img, 0.0, idx,
                          dec.stride, k)
     assert e.value.status == N.FASTOCR_ERR_INVALID
+    for flags in (2, 0x80000000, 3):   # only FASTOCR_SELECTION_FINAL is defined
+        with pytest.raises(N.FastOCRError) as e:
+            N.fastocr_sparse_attend_ex(dec.handle, q, dec.kv[0], case.img_range, idx, dec.stride,
+                                       k, out, flags)
+        assert e.value.status == N.FASTOCR_ERR_INVALID
+
+
+@pytest.mark.parametrize("variant", list(VARIANTS))
+def test_selection_final_flag(variant):
+    """A gather call told that its selection is final (FASTOCR_SELECTION_FINAL:
+    written before the previous kernel began) gives the same outputs, bit for
+    bit, as the call that checks it again after its wait, and reports bad
+    entries the same way."""
+    from dynamic_sparse_kv_gb300 import DecodeAttention
+    from dynamic_sparse_kv_gb300 import _native as N
+    case = _case("qwen7b_b1", batch=3, layers=1, prompt=40, grid=(1, 24, 24), steps=20, tau=0.1)
+    wl = case.wl
+    n_t = wl.seq_len_at(19)
+    dec = DecodeAttention(case.k_cache, case.v_cache, case.block_table, q_heads=wl.q_heads,
+                          img_range=case.img_range, max_img=wl.n_img, tau=wl.tau,
+                          variants=_variants(variant))
+    dec.set_seq_len(n_t)
+    q = case.q_at(19)[0].contiguous()
+    idx = torch.zeros(wl.batch, dec.stride, dtype=torch.int32, device="cuda")
+    k = torch.zeros(wl.batch, dtype=torch.int32, device="cuda")
+    out_f = torch.empty_like(q)
+    N.fastocr_focal_attend(dec.handle, q, dec.kv[0], case.img_range, wl.tau, out_f, idx,
+                           dec.stride, k)
+    torch.cuda.synchronize()
+    outs = []
+    for flags in (0, N.SELECTION_FINAL):
+        o = torch.empty_like(q)
+        N.fastocr_sparse_attend_ex(dec.handle, q, dec.kv[0], case.img_range, idx, dec.stride, k,
+                                   o, flags)
+        torch.cuda.synchronize()
+        outs.append(o)
+    assert torch.equal(outs[0], outs[1])
+    assert dec.device_status() == 0
+    kv = KVCache(case)
+    for b in range(wl.batch):
+        Kl, Vl = kv(0, b)
+        sel = idx[b, :int(k[b])].cpu().numpy()
+        ref = A.sparse_attend(np64(q[b]), Kl, Vl, n_t, wl.prompt, wl.n_img, sel)
+        assert_close(outs[1][b], ref, TOL["bf16"], f"final b={b}")
+    bad = idx.clone()
+    bad[0, 0] = wl.prompt - 1                 # outside the image range
+    for flags in (0, N.SELECTION_FINAL):
+        o = torch.empty_like(q)
+        N.fastocr_sparse_attend_ex(dec.handle, q, dec.kv[0], case.img_range, bad, dec.stride, k,
+                                   o, flags)
+        assert dec.device_status() & N.DEV_BAD_SELECTION
 
 
 def test_read_probe_reads_every_word():
