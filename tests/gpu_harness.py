@@ -104,7 +104,7 @@ def assert_close(gpu: torch.Tensor, ref: np.ndarray, tol: float, where=""):
     return float(err)
 
 
-class GpuRun:
+class CudaDecodeRun:
     """Run the CUDA path step by step, keeping outputs and selections on the host."""
 
     def __init__(self, case, tau=None, focal_layers=None, splits=None, period=None):
@@ -181,7 +181,7 @@ def oracle_inputs(case, kv: KVCache, batch_idx=None):
     return bsel, img, q_of, kv_of, n_t_of
 
 
-def compare_decode(run: GpuRun, steps: int, batch_idx=None, check_focal=True):
+def compare_decode(run: CudaDecodeRun, steps: int, batch_idx=None, check_focal=True):
     """Oracle schedule over steps [0, steps) on sequences batch_idx, continuing
     with the GPU's (validated) selections; compare every output. Returns stats."""
     case, wl = run.case, run.wl

@@ -14,7 +14,7 @@ import torch
 
 import oracle.attention as A
 import synth
-from gpu_harness import TOL, GpuRun, KVCache, assert_close, compare_decode, np64
+from gpu_harness import TOL, CudaDecodeRun, KVCache, assert_close, compare_decode, np64
 
 pytestmark = pytest.mark.gpu
 
@@ -36,7 +36,7 @@ def test_qwen7b_b1_full_size():
     wl = synth.workload("qwen7b_b1")
     n = wl.warmup + 3
     case = synth.make_case(wl, device="cuda", n_steps=n)
-    run = GpuRun(case).run(0, n)
+    run = CudaDecodeRun(case).run(0, n)
     stats = compare_decode(run, n)
     assert len(stats["focal"]) == 3
     del case, run
@@ -47,7 +47,7 @@ def test_serving_b32_full_size_sampled():
     wl = synth.workload("serving_b32", warmup=2)
     n = wl.warmup + 2
     case = synth.make_case(wl, device="cuda", n_steps=n)
-    run = GpuRun(case).run(0, n)
+    run = CudaDecodeRun(case).run(0, n)
     compare_decode(run, n, batch_idx=[0, 17, 31])
     del case, run
     _free()
@@ -58,7 +58,7 @@ def test_multipage_b8_full_size_sampled(tau):
     wl = synth.workload("multipage_b8", warmup=2, tau=tau)
     n = wl.warmup + 1
     case = synth.make_case(wl, device="cuda", n_steps=n)
-    run = GpuRun(case).run(0, n)
+    run = CudaDecodeRun(case).run(0, n)
     compare_decode(run, n, batch_idx=[0, 5])
     del case, run
     _free()
@@ -71,7 +71,7 @@ def test_multipage_b8_last_step(tau):
     wl = synth.workload("multipage_b8", tau=tau, focal_layers=(9, 18, 27), warmup=0)
     t = wl.steps - 1
     case = synth.make_case(wl, device="cuda", step0=t, n_steps=1)
-    run = GpuRun(case).run(t, t + 1)
+    run = CudaDecodeRun(case).run(t, t + 1)
     kv = KVCache(case)
     n_t = wl.seq_len_at(t)
     q = np64(case.q_at(t))
@@ -98,7 +98,7 @@ def test_rswa_b16_full_size_sampled(T):
     wl = synth.workload("rswa_b16", steps=T)
     t = T - 1
     case = synth.make_case(wl, device="cuda", step0=t, n_steps=1)
-    run = GpuRun(case).run(t, t + 1, kind="rswa")
+    run = CudaDecodeRun(case).run(t, t + 1, kind="rswa")
     kv = KVCache(case)
     n_t = wl.seq_len_at(t)
     q = np64(case.q_at(t))

@@ -13,7 +13,7 @@ import torch
 
 import oracle.attention as A
 import synth
-from gpu_harness import TOL, GpuRun, KVCache, assert_close, check_selection, compare_decode, np64
+from gpu_harness import TOL, CudaDecodeRun, KVCache, assert_close, check_selection, compare_decode, np64
 
 pytestmark = pytest.mark.gpu
 
@@ -34,7 +34,7 @@ def _case(name, **kw):
 def test_tiny_f32_whole_decode():
     """Tiny fp32 workload, all 32 steps: layer 1 focal, layer 0 reuses F_last."""
     case = _case("tiny_f32")
-    run = GpuRun(case).run(0, case.wl.steps)
+    run = CudaDecodeRun(case).run(0, case.wl.steps)
     stats = compare_decode(run, case.wl.steps)
     assert stats["swaps"] == 0
 
@@ -47,7 +47,7 @@ def test_tiny_f32_whole_decode():
 def test_qwen_shaped_decode(variant):
     """GQA group 7, d=128, bf16, warm-up chooses C, then steady steps."""
     case = _case("qwen7b_b1", **variant)
-    run = GpuRun(case).run(0, case.wl.steps)
+    run = CudaDecodeRun(case).run(0, case.wl.steps)
     compare_decode(run, case.wl.steps)
 
 
@@ -61,14 +61,14 @@ def test_qwen_shaped_decode(variant):
 def test_head_shapes(shape):
     case = _case("qwen7b_b1", batch=2, layers=3, prompt=21, grid=(1, 10, 17), steps=6,
                  warmup=2, n_focal=1, tau=0.1, **shape)
-    run = GpuRun(case).run(0, case.wl.steps)
+    run = CudaDecodeRun(case).run(0, case.wl.steps)
     compare_decode(run, case.wl.steps)
 
 
 def test_serving_shaped_random_start():
     case = _case("serving_b32", batch=5, layers=3, prompt=37, grid=(1, 12, 20), steps=6,
                  warmup=2, n_focal=1)
-    run = GpuRun(case).run(0, case.wl.steps)
+    run = CudaDecodeRun(case).run(0, case.wl.steps)
     compare_decode(run, case.wl.steps)
 
 
@@ -76,7 +76,7 @@ def test_serving_shaped_random_start():
 def test_multipage_tau_sweep(tau):
     case = _case("multipage_b8", batch=3, layers=3, prompt=20, grid=(4, 8, 8), steps=7,
                  warmup=2, n_focal=2, tau=tau)
-    run = GpuRun(case).run(0, case.wl.steps)
+    run = CudaDecodeRun(case).run(0, case.wl.steps)
     compare_decode(run, case.wl.steps)
 
 
@@ -84,8 +84,8 @@ def test_tau_one_equals_dense_on_gpu():
     """Invariant: with tau = 1 every layer's output equals full attention."""
     case = _case("qwen7b_b1", batch=2, layers=4, prompt=33, grid=(1, 8, 24), steps=5,
                  warmup=2, n_focal=2, tau=1.0)
-    run = GpuRun(case).run(0, case.wl.steps)
-    dense = GpuRun(case).run(0, case.wl.steps, kind="dense")
+    run = CudaDecodeRun(case).run(0, case.wl.steps)
+    dense = CudaDecodeRun(case).run(0, case.wl.steps, kind="dense")
     for t in range(case.wl.steps):
         d = (run.outs[t].float() - dense.outs[t].float()).abs().max().item()
         assert d <= 2e-2, (t, d)
@@ -97,8 +97,8 @@ def test_rswa_small():
     wl = synth.workload("rswa_b16", batch=3, layers=2, rswa_prefix=100, prompt=100,
                         rswa_window=16, steps=40)
     case = synth.make_case(wl, device="cuda")
-    run = GpuRun(case).run(0, wl.steps, kind="rswa")
-    dense = GpuRun(case).run(0, wl.steps, kind="dense")
+    run = CudaDecodeRun(case).run(0, wl.steps, kind="rswa")
+    dense = CudaDecodeRun(case).run(0, wl.steps, kind="dense")
     kv = KVCache(case)
     for t in range(wl.steps):
         n_t = wl.seq_len_at(t)
@@ -214,7 +214,7 @@ def test_adaptive_reprofiling():
             m = K.float().mean(0)
             u = m / m.norm(dim=-1, keepdim=True)
             case.q[period - case.step0:, l, b] = (40.0 * u).repeat_interleave(g, 0).to(case.q.dtype)
-    run = GpuRun(case, period=period).run(0, wl.steps)
+    run = CudaDecodeRun(case, period=period).run(0, wl.steps)
     compare_decode(run, wl.steps)
     hist = run.focal_history
     assert [t for t, _ in hist] == [wl.warmup - 1 + m * period for m in range(3)]
@@ -231,20 +231,20 @@ def test_checkpoint_resume():
     case = _case("qwen7b_b1", batch=2, layers=5, prompt=24, grid=(1, 12, 16), steps=14,
                  warmup=4, n_focal=2, tau=0.1)
     wl = case.wl
-    whole = GpuRun(case).run(0, wl.steps)
+    whole = CudaDecodeRun(case).run(0, wl.steps)
     t1, t2 = 2, 9                                  # inside the warm-up; steady decode
-    part = GpuRun(case).run(0, t1)
+    part = CudaDecodeRun(case).run(0, t1)
     st = part.dec.state_dict()
     assert st["warm"] is not None and st["focal"] == ()
     assert len(st["warm"][2]) == wl.layers and all(m > 0 for m in st["warm"][2])
     part.dec.close()
-    res = GpuRun(case)
+    res = CudaDecodeRun(case)
     res.dec.load_state_dict(st)
     res.run(t1, t2)
     st2 = res.dec.state_dict()
     assert st2["focal"] == whole.focal and st2["has_f_last"]
     res.dec.close()
-    res2 = GpuRun(case)
+    res2 = CudaDecodeRun(case)
     res2.dec.load_state_dict(st2)
     res2.focal = tuple(st2["focal"])
     res2.run(t2, wl.steps)
@@ -256,7 +256,7 @@ def test_checkpoint_resume():
                 assert np.array_equal(got.sels[t][l][b], sel[b]), f"step {t} layer {l} seq {b}"
     compare_decode(whole, wl.steps)
     with pytest.raises(ValueError):
-        bad = GpuRun(case, tau=0.2)
+        bad = CudaDecodeRun(case, tau=0.2)
         bad.dec.load_state_dict(st2)
 
 
@@ -691,7 +691,7 @@ def test_score_reduce_path_whole_decode():
     case = _case("qwen7b_b1", batch=2, layers=5, prompt=40, grid=(1, 16, 24), steps=12,
                  warmup=3, n_focal=2)
     calls = []
-    run = GpuRun(case)
+    run = CudaDecodeRun(case)
     run.dec.score_reduce = lambda sigma: calls.append(sigma.shape)
     run.dec.sigma = torch.zeros(case.wl.batch, case.wl.n_img, dtype=torch.float32, device="cuda")
     run.run(0, case.wl.steps)
@@ -753,12 +753,12 @@ def test_page_sizes(page):
     are right at every size."""
     case = _case("qwen7b_b1", batch=2, layers=3, prompt=21, grid=(1, 10, 17), steps=6,
                  warmup=2, n_focal=1, tau=0.1, page_size=page)
-    run = GpuRun(case).run(0, case.wl.steps)
+    run = CudaDecodeRun(case).run(0, case.wl.steps)
     compare_decode(run, case.wl.steps)
     wl = synth.workload("rswa_b16", batch=2, layers=1, rswa_prefix=70, prompt=70,
                         rswa_window=9, steps=30, page_size=page)
     rcase = synth.make_case(wl, device="cuda")
-    rrun = GpuRun(rcase).run(0, wl.steps, kind="rswa")
+    rrun = CudaDecodeRun(rcase).run(0, wl.steps, kind="rswa")
     kv = KVCache(rcase)
     for t in (0, 8, 9, 29):
         n_t = wl.seq_len_at(t)
