@@ -468,7 +468,7 @@ class Bench:
         def only(kind):
             def fn(q, out, stream=None):
                 cur = dec.sel[max(dec.focal)]
-                fresh = True   # as in the step: re-check the selection after a focal layer
+                flags = 0   # the same flags as the step's calls
                 for l in range(dec.layers):
                     if l in focal:
                         idx, k = dec.sel[l]
@@ -477,12 +477,12 @@ class Bench:
                                                    dec.tau, out[l], idx, dec.stride, k, -1,
                                                    stream)
                         cur = (idx, k)
-                        fresh = True
+                        flags = N.SELECTION_PENDING
                     elif kind == "sparse":
                         N.fastocr_sparse_attend_ex(dec.handle, q[l], dec.kv[l], dec.img_range,
-                                                   cur[0], dec.stride, cur[1], out[l],
-                                                   0 if fresh else N.SELECTION_FINAL, stream)
-                        fresh = False
+                                                   cur[0], dec.stride, cur[1], out[l], flags,
+                                                   stream)
+                        flags = N.SELECTION_FINAL
             return fn
         n_f = len(focal)
         return {"focal": (only("focal"), n_f, 2 * n_f),

@@ -175,7 +175,8 @@ def fastocr_sparse_attend(handle, q, kv: fastocr_kv, img_range, idx, idx_stride,
                                      _stream(stream)))
 
 
-SELECTION_FINAL = 1   # FASTOCR_SELECTION_FINAL
+SELECTION_FINAL = 1     # FASTOCR_SELECTION_FINAL
+SELECTION_PENDING = 2   # FASTOCR_SELECTION_PENDING
 
 
 def fastocr_sparse_attend_ex(handle, q, kv: fastocr_kv, img_range, idx, idx_stride, k, out,

@@ -320,13 +320,15 @@ fastocr_status fastocr_sparse_attend_ex(fastocr_handle* h, const void* q, const 
   fastocr_status st = check_kv(h, kv);
   if (st != FASTOCR_OK) return st;
   if (!aligned16(q) || !aligned16(out)) return FASTOCR_ERR_ALIGN;
-  if (idx_stride < 1 || (flags & ~(uint32_t)FASTOCR_SELECTION_FINAL)) return FASTOCR_ERR_INVALID;
+  const uint32_t known = FASTOCR_SELECTION_FINAL | FASTOCR_SELECTION_PENDING;
+  if (idx_stride < 1 || (flags & ~known) || (flags & known) == known) return FASTOCR_ERR_INVALID;
   Params p = base_params(h, q, kv, out);
   p.img_range = img_range;
   p.idx = idx;
   p.idx_stride = idx_stride;
   p.k_in = k;
   p.sel_final = (flags & FASTOCR_SELECTION_FINAL) ? 1 : 0;
+  p.sel_pending = (flags & FASTOCR_SELECTION_PENDING) ? 1 : 0;
   // text tokens (cache minus the image) plus at most idx_stride selected ones
   const long text = std::max(0L, expected_tokens(h) - (long)h->dims.max_img_tokens);
   return launch(h, kSparse, std::min(expected_tokens(h), text + idx_stride), p, stream);

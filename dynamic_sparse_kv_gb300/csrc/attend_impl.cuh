@@ -491,7 +491,13 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
   int pre_issued = 0;   // leading tiles of this warp already staged
   int spec_u1 = n_txt_pad;   // speculative selection entries: [n_txt_pad, spec_u1)
   int spec_raw[kPer];
-  if (MODE == kSparse) {
+  // A selection that the previous kernel is still writing is not read before
+  // the wait: only the text is staged, and the selection is laid out after
+  // it. Only the general variant does so: its pipeline holds a few of a
+  // CTA's tiles, so a stale guess costs a drain and a full restart, while the
+  // deep variant's small grids stage whole lists and measured faster guessing.
+  const bool sel_pending = MODE == kSparse && V == kGeneral && p.sel_pending;
+  if (MODE == kSparse && !sel_pending) {
     // One thread reads k and the CTA shares that reading: the previous kernel
     // may be writing k, and threads that saw different values would lay out
     // (and stage) the list differently.
@@ -580,7 +586,7 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
   // selection, all in flight together. The tile follows the staged ones in
   // its warp's order (sparse: under the speculative layout, redone below if
   // the speculation fails).
-  if (c.has_cur && n_pre < kSliceMax) {
+  if (c.has_cur && n_pre < kSliceMax && !sel_pending) {
     const int t_cur = n_pre / kTile;   // n_pre is a multiple of kTile here
     if (warp == t_cur % kWarps && pre_issued == t_cur / kWarps && pre_issued < ST) {
       issue(pre_issued, n_pre + 1);
@@ -601,7 +607,16 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
     }
   }
   bool relaid = false;   // the selection's rows were resolved again (CTA-uniform)
-  if (MODE == kSparse && p.sel_final) {
+  if (sel_pending) {
+    // the selection is final now: lay it out behind the text and resolve its
+    // rows (and the current token's, which moves behind it); the text tiles
+    // staged before the wait stay where they are
+    const int k = __ldcg(p.k_in + b);
+    add_selection(p, k, split, c, bad);
+    n_sel_pad = (c.n_sel + kTile - 1) / kTile * kTile;
+    resolve(0, n_txt_pad, min(n_txt_pad + n_sel_pad + c.has_cur, kSliceMax));
+    relaid = true;
+  } else if (MODE == kSparse && p.sel_final) {
     // the caller guarantees that k and idx were written before the previous
     // kernel began, so the reading before the wait is the real selection:
     // only report its faulty entries (each thread its own, no barrier)

@@ -76,6 +76,7 @@ struct Params {
   int idx_stride;
   const int32_t* k_in;       // sparse: [B]
   int sel_final;             // sparse: idx and k_in were final before the previous kernel began
+  int sel_pending;           // sparse: the previous kernel writes idx and k_in (no early staging)
   int32_t* idx_out;          // focal: [B, idx_stride]
   int32_t* k_out;            // focal: [B]
   double tau;

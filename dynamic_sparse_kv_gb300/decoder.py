@@ -273,26 +273,27 @@ class DecodeAttention:
     def step(self, q, out, stream=None):
         """One steady FastOCR decode step over all layers (q, out: [L, B, H_q, d]).
 
-        A gather layer whose selection was written by the kernel right before
-        it (the first after a focal layer, and the step's first layer, which
-        may follow the previous step's last selection) checks it again after
-        its wait; the others are told it is final (FASTOCR_SELECTION_FINAL)."""
+        The first gather layer after a focal layer is told that the kernel
+        right before it writes its selection (FASTOCR_SELECTION_PENDING: it
+        lays the selection out after its wait); the step's first layer, which
+        may follow the previous step's last selection kernel, checks the
+        selection it staged early; every other gather layer is told that its
+        selection is final (FASTOCR_SELECTION_FINAL)."""
         cur = self.sel[max(self.focal)] if self.has_f_last else None
-        fresh = True   # cur may have been written by the kernel before the next launch
+        flags = 0   # first layer: stage F_last early, check it after the wait
         for l in range(self.layers):
             if l in self.sel:
                 idx, k = self.sel[l]
                 self.focal_layer(l, q[l], out[l], idx, k, stream)
                 cur = (idx, k)
-                fresh = True
+                flags = N.SELECTION_PENDING
             elif cur is None:
                 N.fastocr_full_attend(self.handle, q[l], self.kv[l], out[l], stream)
-                fresh = False
+                flags = N.SELECTION_FINAL
             else:
                 N.fastocr_sparse_attend_ex(self.handle, q[l], self.kv[l], self.img_range, cur[0],
-                                           self.stride, cur[1], out[l],
-                                           0 if fresh else N.SELECTION_FINAL, stream)
-                fresh = False
+                                           self.stride, cur[1], out[l], flags, stream)
+                flags = N.SELECTION_FINAL
         self.has_f_last = True
 
     def dense_step(self, q, out, stream=None):

@@ -208,8 +208,15 @@ fastocr_status fastocr_sparse_attend(fastocr_handle* h, const void* q, const fas
  * The kernel then takes the selection it reads before the wait as final and
  * skips re-reading it after the wait (and the CTA barrier that check needs).
  * With the flag set and the guarantee broken, the layer may attend a stale
- * selection; nothing faults. Other flag bits: FASTOCR_ERR_INVALID. */
+ * selection; nothing faults. FASTOCR_SELECTION_PENDING: a hint that the kernel
+ * right before this call writes idx and k (e.g. the selection of the focal
+ * layer just before): large grids then stage only the text before the wait
+ * and lay the selection out after it, instead of staging the selection they
+ * read early, which would be the previous one, and redoing it; small grids
+ * (whole lists staged early) ignore it. Results do not depend on it. Both
+ * flags, or any other bit: FASTOCR_ERR_INVALID. */
 #define FASTOCR_SELECTION_FINAL 1u
+#define FASTOCR_SELECTION_PENDING 2u
 fastocr_status fastocr_sparse_attend_ex(fastocr_handle* h, const void* q, const fastocr_kv* kv,
                                         const int32_t* img_range, const int32_t* idx,
                                         int32_t idx_stride, const int32_t* k, void* out,

@@ -471,7 +471,7 @@ def test_host_argument_errors():
         N.fastocr_select(dec.handle, dec.kv[0], case.img_range, sigma, case.wl.n_img, 0.0, idx,
                          dec.stride, k)
     assert e.value.status == N.FASTOCR_ERR_INVALID
-    for flags in (2, 0x80000000, 3):   # only FASTOCR_SELECTION_FINAL is defined
+    for flags in (4, 0x80000000, 3):   # FINAL and PENDING exclude each other; no other bits
         with pytest.raises(N.FastOCRError) as e:
             N.fastocr_sparse_attend_ex(dec.handle, q, dec.kv[0], case.img_range, idx, dec.stride,
                                        k, out, flags)
@@ -481,9 +481,10 @@ def test_host_argument_errors():
 @pytest.mark.parametrize("variant", list(VARIANTS))
 def test_selection_final_flag(variant):
     """A gather call told that its selection is final (FASTOCR_SELECTION_FINAL:
-    written before the previous kernel began) gives the same outputs, bit for
-    bit, as the call that checks it again after its wait, and reports bad
-    entries the same way."""
+    written before the previous kernel began) or pending (FASTOCR_SELECTION_
+    PENDING: laid out only after the wait) gives the same outputs, bit for
+    bit, as the call that stages it early and checks it after its wait, and
+    reports bad entries the same way."""
     from dynamic_sparse_kv_gb300 import DecodeAttention
     from dynamic_sparse_kv_gb300 import _native as N
     case = _case("qwen7b_b1", batch=3, layers=1, prompt=40, grid=(1, 24, 24), steps=20, tau=0.1)
@@ -501,13 +502,13 @@ def test_selection_final_flag(variant):
                            dec.stride, k)
     torch.cuda.synchronize()
     outs = []
-    for flags in (0, N.SELECTION_FINAL):
+    for flags in (0, N.SELECTION_FINAL, N.SELECTION_PENDING):
         o = torch.empty_like(q)
         N.fastocr_sparse_attend_ex(dec.handle, q, dec.kv[0], case.img_range, idx, dec.stride, k,
                                    o, flags)
         torch.cuda.synchronize()
         outs.append(o)
-    assert torch.equal(outs[0], outs[1])
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
     assert dec.device_status() == 0
     kv = KVCache(case)
     for b in range(wl.batch):
@@ -517,7 +518,7 @@ def test_selection_final_flag(variant):
         assert_close(outs[1][b], ref, TOL["bf16"], f"final b={b}")
     bad = idx.clone()
     bad[0, 0] = wl.prompt - 1                 # outside the image range
-    for flags in (0, N.SELECTION_FINAL):
+    for flags in (0, N.SELECTION_FINAL, N.SELECTION_PENDING):
         o = torch.empty_like(q)
         N.fastocr_sparse_attend_ex(dec.handle, q, dec.kv[0], case.img_range, bad, dec.stride, k,
                                    o, flags)
