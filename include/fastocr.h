@@ -78,7 +78,10 @@
 extern "C" {
 #endif
 
-#define FASTOCR_ABI_VERSION 1
+/* 2 adds fastocr_focal_scores, fastocr_select, fastocr_set_variant,
+ * fastocr_read_probe, fastocr_profiler_read / fastocr_profiler_load and
+ * fastocr_sparse_attend_ex to version 1; no call of version 1 changed. */
+#define FASTOCR_ABI_VERSION 2
 
 typedef struct fastocr_handle fastocr_handle;
 typedef void* fastocr_stream; /* cudaStream_t */

@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_status_strings(lib):
     from dynamic_sparse_kv_gb300 import _native as N
-    assert N.fastocr_abi_version() == 1
+    assert N.fastocr_abi_version() == 2
     for s in (0, -1, -2, -3, -4, -5, -6):
         assert N.status_string(s) and N.status_string(s) != "unknown status"
     assert N.status_string(123) == "unknown status"
