@@ -457,7 +457,6 @@ class Bench:
 
     # ---- per-kind graphs: the step's layers of one kind, in step order
     def kind_fns(self, dec):
-        import dynamic_sparse_kv_gb300._native as N
         wl = self.wl
         if self.kind == "rswa":
             def rswa(q, out, stream=None):
@@ -465,24 +464,9 @@ class Bench:
             return {"rswa": (rswa, dec.layers, dec.layers)}
         focal = set(dec.sel)
 
-        def only(kind):
+        def only(kind):   # the step's own schedule, issuing just this kind's calls
             def fn(q, out, stream=None):
-                cur = dec.sel[max(dec.focal)]
-                flags = 0   # the same flags as the step's calls
-                for l in range(dec.layers):
-                    if l in focal:
-                        idx, k = dec.sel[l]
-                        if kind == "focal":
-                            N.fastocr_focal_attend(dec.handle, q[l], dec.kv[l], dec.img_range,
-                                                   dec.tau, out[l], idx, dec.stride, k, -1,
-                                                   stream)
-                        cur = (idx, k)
-                        flags = N.SELECTION_PENDING
-                    elif kind == "sparse":
-                        N.fastocr_sparse_attend_ex(dec.handle, q[l], dec.kv[l], dec.img_range,
-                                                   cur[0], dec.stride, cur[1], out[l], flags,
-                                                   stream)
-                        flags = N.SELECTION_FINAL
+                dec.step(q, out, stream, only=kind)
             return fn
         n_f = len(focal)
         return {"focal": (only("focal"), n_f, 2 * n_f),

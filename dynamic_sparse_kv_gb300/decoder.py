@@ -270,7 +270,7 @@ class DecodeAttention:
         N.fastocr_select(self.handle, self.kv[l], self.img_range, self.sigma,
                          self.sigma.shape[1], self.tau, idx, self.stride, k, stream)
 
-    def step(self, q, out, stream=None):
+    def step(self, q, out, stream=None, only=None):
         """One steady FastOCR decode step over all layers (q, out: [L, B, H_q, d]).
 
         The first gather layer after a focal layer is told that the kernel
@@ -278,23 +278,30 @@ class DecodeAttention:
         lays the selection out after its wait); the step's first layer, which
         may follow the previous step's last selection kernel, checks the
         selection it staged early; every other gather layer is told that its
-        selection is final (FASTOCR_SELECTION_FINAL)."""
+        selection is final (FASTOCR_SELECTION_FINAL).
+
+        only="focal" / "sparse": issue just that kind's calls, with the same
+        flags (per-kind timing)."""
         cur = self.sel[max(self.focal)] if self.has_f_last else None
         flags = 0   # first layer: stage F_last early, check it after the wait
         for l in range(self.layers):
             if l in self.sel:
                 idx, k = self.sel[l]
-                self.focal_layer(l, q[l], out[l], idx, k, stream)
+                if only != "sparse":
+                    self.focal_layer(l, q[l], out[l], idx, k, stream)
                 cur = (idx, k)
                 flags = N.SELECTION_PENDING
+                continue
+            if only == "focal":
+                pass
             elif cur is None:
                 N.fastocr_full_attend(self.handle, q[l], self.kv[l], out[l], stream)
-                flags = N.SELECTION_FINAL
             else:
                 N.fastocr_sparse_attend_ex(self.handle, q[l], self.kv[l], self.img_range, cur[0],
                                            self.stride, cur[1], out[l], flags, stream)
-                flags = N.SELECTION_FINAL
-        self.has_f_last = True
+            flags = N.SELECTION_FINAL
+        if only is None:
+            self.has_f_last = True
 
     def dense_step(self, q, out, stream=None):
         for l in range(self.layers):

@@ -222,6 +222,42 @@ def test_adaptive_reprofiling():
     assert not set(hist[1][1]) & set(first)
 
 
+@pytest.mark.parametrize("focal", [(1, 2, 4), (0, 1, 2, 3)])
+def test_fixed_adjacent_focal_layers_and_graph(focal):
+    """Focal sets with adjacent layers (a focal layer whose selection no
+    gather layer uses before the next focal layer selects again): every output
+    and every selection of the whole decode matches the oracle, and a
+    CUDA-graph replay of the step gives the eager step's outputs and
+    selections bit for bit from the same starting selections."""
+    from dynamic_sparse_kv_gb300 import CapturedStep
+    case = _case("qwen7b_b1", batch=2, layers=6, prompt=24, grid=(1, 12, 16), steps=10,
+                 tau=0.1, warmup=0, focal_layers=focal)
+    wl = case.wl
+    run = CudaDecodeRun(case).run(0, wl.steps)
+    assert run.dec.launches_per_step("fastocr") == wl.layers + len(focal)
+    compare_decode(run, wl.steps)
+    t = wl.steps - 1
+    dec = run.dec
+    cap = CapturedStep(dec)
+    snap = {l: (i.clone(), k.clone()) for l, (i, k) in dec.sel.items()}   # F_last included
+    dec.set_seq_len(wl.seq_len_at(t))
+    cap.q.copy_(case.q_at(t))
+    cap.replay()
+    torch.cuda.synchronize()
+    got = cap.out.clone()
+    got_sel = {l: (i.clone(), k.clone()) for l, (i, k) in dec.sel.items()}
+    for l, (i, k) in dec.sel.items():         # the same starting selections for the eager step
+        i.copy_(snap[l][0])
+        k.copy_(snap[l][1])
+    out2 = torch.empty_like(cap.out)
+    dec.step(case.q_at(t).contiguous(), out2)
+    torch.cuda.synchronize()
+    assert torch.equal(out2, got)
+    for l, (i, k) in dec.sel.items():
+        assert torch.equal(k, got_sel[l][1]) and torch.equal(i, got_sel[l][0]), l
+    assert dec.device_status() == 0
+
+
 def test_checkpoint_resume():
     """The method's state saved mid-warm-up and again in the steady decode and
     loaded into fresh decoders: the resumed decode gives the same outputs and
