@@ -60,7 +60,9 @@
  *  expects before that kernel completes, so if img_range contains the
  *  current token N_t - 1 (the image normally ends before the generated
  *  text), that token's K/V must be written before the preceding kernel
- *  starts as well.
+ *  starts as well. fastocr_sparse_attend_ex's flags change when the
+ *  selection is read: FASTOCR_SELECTION_FINAL reads it only before the wait,
+ *  FASTOCR_SELECTION_PENDING (large grids) only after it.
  *
  *  Errors: argument errors are detected on the host and returned as a
  *  negative status before anything is launched. Faults in device data (page
