@@ -378,6 +378,34 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
   if (p.splits > 1) cluster_arrive_relaxed();
 
   int bad = 0;
+  // A selection that the previous kernel is still writing is not read before
+  // the wait: only the text is staged, and the selection is laid out after
+  // it. Only the general variant does so: its pipeline holds a few of a
+  // CTA's tiles, so a stale guess costs a drain and a full restart, while the
+  // deep variant's small grids stage whole lists and measured faster guessing.
+  const bool sel_pending = MODE == kSparse && V == kGeneral && p.sel_pending;
+  // Otherwise k and this CTA's share of the selection are read before the
+  // wait (checked after it unless the caller declared them final), issued
+  // together with the lengths' loads. The share is guessed from the keep
+  // capacity (k = idx_stride, the usual case); a wrong guess costs one more
+  // round of loads below.
+  constexpr int kPer = kSliceMax / kThreads;   // entries a thread resolves
+  int spec_raw[kPer];   // selection entry v = tid + j*kThreads of the share
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) spec_raw[j] = -1;
+  int k_ld = 0, lo_g = 0, n_g = 0;
+  if (MODE == kSparse && !sel_pending) {
+    const int per_g = (p.idx_stride + p.splits - 1) / p.splits;
+    lo_g = split * per_g;
+    n_g = max(0, min(per_g, p.idx_stride - lo_g));
+    const int32_t* sel_b = p.idx + (size_t)b * p.idx_stride;
+    if (tid == 0) k_ld = __ldcg(p.k_in + b);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int v = tid + j * kThreads;
+      spec_raw[j] = v < n_g ? __ldcg(sel_b + lo_g + v) : -1;
+    }
+  }
   CtaList c = make_cta_list<MODE>(p, b, split, bad);
 
   // Work list of this CTA: [text, padded to whole tiles][selection, padded to
@@ -410,7 +438,6 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
   // (page*H_kv + hkv)*page_size + slot (-1: masked) and positions; every
   // lookup of a thread is issued before any is used.
   auto resolve = [&](int rb, int u0, int u1) {
-    constexpr int kPer = kSliceMax / kThreads;
     int pos[kPer], page[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
@@ -481,93 +508,116 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
   };
 
   // ---------------- before the previous kernel completes
-  // Rows of round 0: the text, the selection (sparse; speculative, since the
-  // previous kernel may still be writing k and idx) and the current token
-  // (its row is final now, its K/V may not be). Then every whole tile of this
-  // warp that the pipeline holds, up to but excluding the current token's.
-  constexpr int kPer = kSliceMax / kThreads;
+  // Rows of round 0: the text, the selection (sparse; read before the wait)
+  // and the current token (its row is final now, its K/V may not be), with
+  // all their page lookups in one round. Then every whole tile of this warp
+  // that the pipeline holds, up to but excluding the current token's.
   const int n_txt0 = min(n_txt_pad, kSliceMax);
-  resolve(0, 0, n_txt0);
   int pre_issued = 0;   // leading tiles of this warp already staged
-  int spec_u1 = n_txt_pad;   // speculative selection entries: [n_txt_pad, spec_u1)
-  int spec_raw[kPer];
-  // A selection that the previous kernel is still writing is not read before
-  // the wait: only the text is staged, and the selection is laid out after
-  // it. Only the general variant does so: its pipeline holds a few of a
-  // CTA's tiles, so a stale guess costs a drain and a full restart, while the
-  // deep variant's small grids stage whole lists and measured faster guessing.
-  const bool sel_pending = MODE == kSparse && V == kGeneral && p.sel_pending;
+  int spec_u1 = n_txt_pad;   // selection entries read before the wait: [n_txt_pad, spec_u1)
   if (MODE == kSparse && !sel_pending) {
-    // One thread reads k and the CTA shares that reading: the previous kernel
+    // One thread's reading of k is shared by the CTA: the previous kernel
     // may be writing k, and threads that saw different values would lay out
     // (and stage) the list differently.
     int* s_spec_k = reinterpret_cast<int*>(smem + SM::kSpecK);
-    if (tid == 0) *s_spec_k = __ldcg(p.k_in + b);
+    if (tid == 0) *s_spec_k = k_ld;
     __syncthreads();
     const int k_cap = min(c.n_img, p.idx_stride);
     const int spec_k = min(max(*s_spec_k, 0), k_cap);
     const int per = (spec_k + p.splits - 1) / p.splits;
     c.sel_lo = split * per;
     c.n_sel = max(0, min(per, spec_k - c.sel_lo));
+    if (c.sel_lo != lo_g || c.n_sel > n_g) {   // CTA-uniform: the guessed share missed
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int v = tid + j * kThreads;
+        spec_raw[j] = v < c.n_sel ? __ldcg(c.sel + c.sel_lo + v) : -1;
+      }
+    }
     n_sel_pad = (c.n_sel + kTile - 1) / kTile * kTile;
     spec_u1 = min(kSliceMax, n_txt_pad + c.n_sel);
-    const int u_pad = min(kSliceMax, n_txt_pad + n_sel_pad);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+      if (n_txt_pad + tid + j * kThreads >= spec_u1) spec_raw[j] = -1;
+  }
+  const int n_pre = min(kSliceMax, n_txt_pad + n_sel_pad);   // entries before the current token
+  {
     const int u_staged = kWarps * ST * kTile;   // entries the pre-wait tiles can cover
-    int pos[kPer], page[kPer];
+    int tpos[kPer], tpage[kPer], sps[kPer], spage[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-      const int u = n_txt_pad + tid + j * kThreads;
-      spec_raw[j] = u < spec_u1 ? __ldcg(c.sel + c.sel_lo + (u - n_txt_pad)) : -1;
-      pos[j] = (u < spec_u1 && spec_raw[j] >= c.img_start && spec_raw[j] < c.img_start + c.n_img)
-                   ? spec_raw[j] : -1;
+      const int u = tid + j * kThreads;
+      tpos[j] = u < n_txt0 ? pos_of(u) : -1;   // text entries: no memory reads
+      const int r = spec_raw[j];
+      sps[j] = (MODE == kSparse && r >= c.img_start && r < c.img_start + c.n_img) ? r : -1;
     }
+    const bool cur_here = c.has_cur && tid == 0 && n_pre < kSliceMax;
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) page[j] = pos[j] >= 0 ? __ldcg(bt + (pos[j] >> p.log2_page)) : -1;
+    for (int j = 0; j < kPer; ++j) tpage[j] = tpos[j] >= 0 ? __ldcg(bt + (tpos[j] >> p.log2_page)) : -1;
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int u = n_txt_pad + tid + j * kThreads;
-      if (u >= u_pad) continue;
-      int row = -1, ps = pos[j];
-      if (ps >= 0 && page[j] >= 0 && page[j] < p.num_pages) {
-        row = ((page[j] * p.Hkv + hkv) << p.log2_page) | (ps & page_mask);
-        // beyond the staged tiles: pull into L2 for later. Only the general
-        // variant (large grids) does: there it shortens the post-wait stream,
-        // while the deep variant's small grids measured faster without the
-        // extra traffic next to the running layer.
-        if constexpr (V == kGeneral) {
-          if (u >= u_staged) {
-            prefetch_l2(kg + (size_t)row * D, ROWB);
-            prefetch_l2(vg + (size_t)row * D, ROWB);
-          }
+    for (int j = 0; j < kPer; ++j) spage[j] = sps[j] >= 0 ? __ldcg(bt + (sps[j] >> p.log2_page)) : -1;
+    const int cpage = cur_here ? __ldcg(bt + (c.cur_pos >> p.log2_page)) : -1;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {   // text
+      const int u = tid + j * kThreads;
+      if (u >= n_txt0) continue;
+      int row = -1, ps = tpos[j];
+      if (ps >= 0) {
+        if (tpage[j] < 0 || tpage[j] >= p.num_pages) {
+          bad |= kDevBadPage;
+          ps = -1;
+        } else {
+          row = ((tpage[j] * p.Hkv + hkv) << p.log2_page) | (ps & page_mask);
         }
-      } else {
-        ps = -1;
       }
       srow[u] = row;
       spos[u] = ps;
     }
+    if (MODE == kSparse && !sel_pending) {
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {   // selection
+        const int u = n_txt_pad + tid + j * kThreads;
+        if (u >= n_pre) continue;
+        int row = -1, ps = sps[j];
+        if (ps >= 0 && spage[j] >= 0 && spage[j] < p.num_pages) {
+          row = ((spage[j] * p.Hkv + hkv) << p.log2_page) | (ps & page_mask);
+          // beyond the staged tiles: pull into L2 for later. Only the general
+          // variant (large grids) does: there it shortens the post-wait stream,
+          // while the deep variant's small grids measured faster without the
+          // extra traffic next to the running layer.
+          if constexpr (V == kGeneral) {
+            if (u >= u_staged) {
+              prefetch_l2(kg + (size_t)row * D, ROWB);
+              prefetch_l2(vg + (size_t)row * D, ROWB);
+            }
+          }
+        } else {
+          ps = -1;
+        }
+        srow[u] = row;
+        spos[u] = ps;
+      }
+    }
+    if (cur_here) {
+      int row = -1, ps = c.cur_pos;
+      if (cpage >= 0 && cpage < p.num_pages) {
+        row = ((cpage * p.Hkv + hkv) << p.log2_page) | (ps & page_mask);
+        prefetch_l2(kg + (size_t)row * D, ROWB);
+        prefetch_l2(vg + (size_t)row * D, ROWB);
+      } else {
+        bad |= kDevBadPage;
+        ps = -1;
+      }
+      srow[n_pre] = row;
+      spos[n_pre] = ps;
+    }
   }
-  const int n_pre = min(kSliceMax, n_txt_pad + n_sel_pad);   // entries before the current token
   // q and the current token's K/V may still be written by the previous
   // kernel, so they are read only after the wait; pulling their lines into L2
   // now is safe (L2 is where those writes land) and shortens that read.
   if (tid == 0)
     prefetch_l2(static_cast<const T*>(p.q) + ((size_t)b * p.Hq + (size_t)hkv * p.g) * D,
                 p.g * D * (uint32_t)sizeof(T));
-  if (c.has_cur && tid == 0 && n_pre < kSliceMax) {
-    const int page = __ldcg(bt + (c.cur_pos >> p.log2_page));
-    int row = -1, ps = c.cur_pos;
-    if (page >= 0 && page < p.num_pages) {
-      row = ((page * p.Hkv + hkv) << p.log2_page) | (ps & page_mask);
-      prefetch_l2(kg + (size_t)row * D, ROWB);
-      prefetch_l2(vg + (size_t)row * D, ROWB);
-    } else {
-      bad |= kDevBadPage;
-      ps = -1;
-    }
-    srow[n_pre] = row;
-    spos[n_pre] = ps;
-  }
   __syncthreads();
 #pragma unroll 1
   for (int j = 0; j < ST; ++j) {
