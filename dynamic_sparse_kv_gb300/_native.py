@@ -78,6 +78,7 @@ def _load() -> ctypes.CDLL:
         "fastocr_set_variant": ([P, I32, I32], I32),
         "fastocr_set_length_hint": ([P, I32], I32),
         "fastocr_read_probe": ([P, ctypes.c_int64, P, P], I32),
+        "fastocr_copy": ([P, P, ctypes.c_int64, P], I32),
         "fastocr_focal_attend_noalloc": ([ctypes.POINTER(fastocr_dims), P,
                                           ctypes.POINTER(fastocr_kv), P, F64, P, P, I32, P, P, P],
                                          I32),
@@ -255,6 +256,11 @@ def fastocr_focal_attend_noalloc(dims: fastocr_dims, q, kv: fastocr_kv, img_rang
                                             _ptr(img_range), float(tau), _ptr(out), _ptr(idx),
                                             int(idx_stride), _ptr(k_out), _ptr(status),
                                             _stream(stream)))
+
+
+def fastocr_copy(dst, src, nbytes, stream=None) -> None:
+    """Copy nbytes from src to dst with the SMs (device or page-locked host memory)."""
+    _check("fastocr_copy", lib.fastocr_copy(_ptr(dst), _ptr(src), int(nbytes), _stream(stream)))
 
 
 def fastocr_read_probe(src, nbytes, sink, stream=None) -> None:

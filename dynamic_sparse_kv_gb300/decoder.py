@@ -176,13 +176,17 @@ class DecodeAttention:
         self.warm_k = torch.zeros(self.layers, self.batch, dtype=torch.int32, device=dev)
         N.fastocr_profiler_reset(self.handle, stream)
 
-    def warmup_step(self, q, out, stream=None):
+    def warmup_step(self, q, out, stream=None, hook=None):
         """Full attention in every layer, profiling image mass; keeps every layer's
         selection so that F_last can be taken once C is known."""
         for l in range(self.layers):
+            if hook:
+                hook(l, True)
             N.fastocr_focal_attend(self.handle, q[l], self.kv[l], self.img_range, self.tau,
                                    out[l], self.warm_idx[l], self.stride, self.warm_k[l],
                                    profile_layer=l, stream=stream)
+            if hook:
+                hook(l, False)
 
     def finish_warmup(self, n_focal: int, stream=None):
         """Choose C from the profile; F_last = last warm-up selection of max(C)."""
@@ -235,14 +239,18 @@ class DecodeAttention:
         return st
 
     def load_state_dict(self, st: dict, stream=None) -> None:
-        """Resume from state_dict() of a decoder over the same shapes and tau."""
+        """Resume from state_dict() of a decoder over the same shapes and tau.
+        With the same focal set the selection buffers keep their addresses
+        (a CapturedStep of this decoder stays valid); another focal set gets
+        new buffers, so a step must then be captured anew."""
         for key in ("batch", "layers", "stride", "tau", "max_img"):
             if st[key] != getattr(self, key):
                 raise ValueError(f"checkpoint {key}={st[key]!r}, decoder has {getattr(self, key)!r}")
-        if st["focal"]:
-            self.set_focal_layers(st["focal"])
-        else:
-            self.focal, self.sel = (), {}
+        if tuple(st["focal"]) != tuple(self.focal):
+            if st["focal"]:
+                self.set_focal_layers(st["focal"])
+            else:
+                self.focal, self.sel = (), {}
         for l, (idx, k) in st["sel"].items():
             self.sel[l][0].copy_(idx)
             self.sel[l][1].copy_(k)
@@ -270,7 +278,7 @@ class DecodeAttention:
         N.fastocr_select(self.handle, self.kv[l], self.img_range, self.sigma,
                          self.sigma.shape[1], self.tau, idx, self.stride, k, stream)
 
-    def step(self, q, out, stream=None, only=None):
+    def step(self, q, out, stream=None, only=None, hook=None):
         """One steady FastOCR decode step over all layers (q, out: [L, B, H_q, d]).
 
         The first gather layer after a focal layer is told that the kernel
@@ -281,36 +289,50 @@ class DecodeAttention:
         selection is final (FASTOCR_SELECTION_FINAL).
 
         only="focal" / "sparse": issue just that kind's calls, with the same
-        flags (per-kind timing)."""
+        flags (per-kind timing). hook(l, before): called on the host right
+        before and right after layer l's calls are issued (CapturedStep uses
+        it to order per-layer host copies against the layers)."""
         cur = self.sel[max(self.focal)] if self.has_f_last else None
         flags = 0   # first layer: stage F_last early, check it after the wait
         for l in range(self.layers):
+            if hook:
+                hook(l, True)
             if l in self.sel:
                 idx, k = self.sel[l]
                 if only != "sparse":
                     self.focal_layer(l, q[l], out[l], idx, k, stream)
                 cur = (idx, k)
                 flags = N.SELECTION_PENDING
-                continue
-            if only == "focal":
-                pass
-            elif cur is None:
-                N.fastocr_full_attend(self.handle, q[l], self.kv[l], out[l], stream)
             else:
-                N.fastocr_sparse_attend_ex(self.handle, q[l], self.kv[l], self.img_range, cur[0],
-                                           self.stride, cur[1], out[l], flags, stream)
-            flags = N.SELECTION_FINAL
+                if only == "focal":
+                    pass
+                elif cur is None:
+                    N.fastocr_full_attend(self.handle, q[l], self.kv[l], out[l], stream)
+                else:
+                    N.fastocr_sparse_attend_ex(self.handle, q[l], self.kv[l], self.img_range,
+                                               cur[0], self.stride, cur[1], out[l], flags, stream)
+                flags = N.SELECTION_FINAL
+            if hook:
+                hook(l, False)
         if only is None:
             self.has_f_last = True
 
-    def dense_step(self, q, out, stream=None):
+    def dense_step(self, q, out, stream=None, hook=None):
         for l in range(self.layers):
+            if hook:
+                hook(l, True)
             N.fastocr_full_attend(self.handle, q[l], self.kv[l], out[l], stream)
+            if hook:
+                hook(l, False)
 
-    def rswa_step(self, q, out, stream=None):
+    def rswa_step(self, q, out, stream=None, hook=None):
         for l in range(self.layers):
+            if hook:
+                hook(l, True)
             N.fastocr_rswa_attend(self.handle, q[l], self.kv[l], self.rswa_prefix,
                                   self.rswa_window, out[l], stream)
+            if hook:
+                hook(l, False)
 
     def launches_per_step(self, kind: str) -> int:
         """Kernels one step of `kind` launches: one attend kernel per layer,
@@ -335,14 +357,34 @@ class CapturedStep:
     profile accumulation in every layer) or "rswa"; or any name with `fn`, a
     callable fn(q, out, stream) that issues the calls (e.g. a subset of the
     step's layers), and `launches`, the kernels it launches.
+
+    host_io=True (step kinds only) adds page-locked host buffers q_host and
+    out_host, and the graph itself moves the step's queries in and its
+    outputs out: write the queries into q_host, replay(), and out_host holds
+    the outputs once the stream reaches the replay's end. The queries come in
+    through fastocr_copy, a kernel in the step's chain of programmatic
+    dependent launches (the first layer stages its K/V while it runs; a copy
+    node would leave a launch gap before the first layer); the outputs go
+    out on a copy engine of a second stream in chunks of L/2, L/4, … layers
+    (the last chunk one layer), each started when its last layer's calls are
+    done, so only the input copy and the last layer's output copy are not
+    hidden behind attention. (Per-layer input copies, waited for by the
+    layers that read them, measured slower: every cross-stream wait before a
+    kernel costs the step more than the copy it hides.)
     """
 
     def __init__(self, dec: DecodeAttention, kind: str = "fastocr", fn=None,
-                 launches: int | None = None):
+                 launches: int | None = None, host_io: bool = False):
         self.dec, self.kind = dec, kind
         shape = (dec.layers, dec.batch, dec.q_heads, dec.head_dim)
         self.q = torch.zeros(shape, dtype=dec.k_cache.dtype, device=dec.k_cache.device)
         self.out = torch.zeros_like(self.q)
+        self.q_host = self.out_host = None
+        if host_io:
+            if fn is not None:
+                raise ValueError("host_io captures one of the step kinds, not a custom fn")
+            self.q_host = torch.zeros(shape, dtype=self.q.dtype, pin_memory=True)
+            self.out_host = torch.zeros(shape, dtype=self.q.dtype, pin_memory=True)
         if kind == "profile" and dec.warm_idx is None:
             dec.begin_warmup()
         if fn is None:   # otherwise fn(q, out, stream) issues the calls and `launches` counts them
@@ -355,9 +397,49 @@ class CapturedStep:
             fn(self.q, self.out)             # warm run outside the capture
         torch.cuda.current_stream().wait_stream(side)
         self.graph = torch.cuda.CUDAGraph()
+        if host_io:
+            self._copy_out = torch.cuda.Stream()
         with torch.cuda.graph(self.graph):
-            fn(self.q, self.out)
+            if host_io:
+                self._issue_with_host_io(fn)
+            else:
+                fn(self.q, self.out)
         self.launches = launches
+
+    @staticmethod
+    def output_chunks(layers: int) -> list:
+        """Last layer of each output chunk: chunks of half the layers left,
+        the last one a single layer (28 layers: 13, 20, 23, 25, 26, 27)."""
+        ends, a = [], 0
+        while a < layers:
+            n = max(1, (layers - a) // 2)
+            ends.append(a + n - 1)
+            a += n
+        return ends
+
+    def _issue_with_host_io(self, fn):
+        main = torch.cuda.current_stream()
+        s_out = self._copy_out
+        s_out.wait_stream(main)
+        N.fastocr_copy(self.q, self.q_host, self.q.numel() * self.q.element_size())
+        ends = set(self.output_chunks(self.q.shape[0]))
+        done, first = [], [0]
+
+        def hook(l, before):
+            if before or l not in ends:
+                return
+            ev = torch.cuda.Event()
+            ev.record(main)
+            done.append(ev)
+            s_out.wait_event(ev)
+            a = first[0]
+            with torch.cuda.stream(s_out):
+                self.out_host[a:l + 1].copy_(self.out[a:l + 1], non_blocking=True)
+            first[0] = l + 1
+
+        fn(self.q, self.out, hook=hook)
+        main.wait_stream(s_out)
+        self._events = done   # alive as long as the graph
 
     def replay(self):
         self.graph.replay()

@@ -81,8 +81,9 @@ extern "C" {
 #endif
 
 /* 2 adds fastocr_focal_scores, fastocr_select, fastocr_set_variant,
- * fastocr_read_probe, fastocr_profiler_read / fastocr_profiler_load and
- * fastocr_sparse_attend_ex to version 1; no call of version 1 changed. */
+ * fastocr_read_probe, fastocr_copy, fastocr_profiler_read /
+ * fastocr_profiler_load and fastocr_sparse_attend_ex to version 1; no call
+ * of version 1 changed. */
 #define FASTOCR_ABI_VERSION 2
 
 typedef struct fastocr_handle fastocr_handle;
@@ -283,6 +284,23 @@ fastocr_status fastocr_set_splits(fastocr_handle* h, int32_t mode, int32_t split
  * Errors: NULL, INVALID (size), ALIGN, NO_DEVICE, CUDA. */
 fastocr_status fastocr_read_probe(const void* src, int64_t bytes, uint32_t* sink,
                                   fastocr_stream stream);
+
+/* Data-movement utility, not a step of the method: copy `bytes` (a multiple
+ * of 16, >= 0) from src to dst (both 16-byte aligned, not overlapping) with
+ * the SMs, in one kernel on `stream`. It is launched with programmatic
+ * dependent launch: it waits for the kernel before it to complete before it
+ * reads src or writes dst, and lets the next kernel start its pre-wait work
+ * while it copies (the attend kernels read their q only after their wait).
+ * Either pointer may be device memory, managed memory or page-locked host
+ * memory (cudaHostAlloc or cudaHostRegister), which the SMs address through
+ * unified addressing -- over NVLink-C2C on a Grace-Blackwell node, where this
+ * moves a step's queries in faster than a copy engine and without the
+ * launch gap a copy node leaves before the next kernel. Pageable host memory
+ * is refused. The caller guarantees that [ptr, ptr + bytes) lies inside each
+ * allocation. Asynchronous; allocates nothing.
+ * Errors: NULL, INVALID (size, overlap, memory the device cannot address),
+ * ALIGN, NO_DEVICE, CUDA. */
+fastocr_status fastocr_copy(void* dst, const void* src, int64_t bytes, fastocr_stream stream);
 
 /* Override the kernel variant of a mode (0 = full/focal, 1 = sparse,
  * 2 = R-SWA): 0 = automatic (default), 1 = general (6 warps of 2 stages, two

@@ -93,6 +93,17 @@ def test_host_checks_without_gpu(lib):
     for bad in (0, 8, 24, -16):
         assert L.fastocr_read_probe(addr, bad, ctypes.byref(sink), None) == N.FASTOCR_ERR_INVALID
     assert L.fastocr_read_probe(addr + 4, 32, ctypes.byref(sink), None) == N.FASTOCR_ERR_ALIGN
+    # so does the SM copy: NULL, size, alignment and overlap before any CUDA call
+    big = (ctypes.c_uint8 * 256)()
+    a = (ctypes.addressof(big) + 15) // 16 * 16
+    assert L.fastocr_copy(None, a, 32, None) == N.FASTOCR_ERR_NULL
+    assert L.fastocr_copy(a, None, 32, None) == N.FASTOCR_ERR_NULL
+    for bad in (8, 24, -16):
+        assert L.fastocr_copy(a + 128, a, bad, None) == N.FASTOCR_ERR_INVALID
+    assert L.fastocr_copy(a + 132, a, 32, None) == N.FASTOCR_ERR_ALIGN
+    assert L.fastocr_copy(a + 128, a + 4, 32, None) == N.FASTOCR_ERR_ALIGN
+    assert L.fastocr_copy(a + 16, a, 32, None) == N.FASTOCR_ERR_INVALID   # overlapping
+    assert L.fastocr_copy(a, a + 16, 32, None) == N.FASTOCR_ERR_INVALID
 
 
 def test_create_without_gpu_reports_no_device(lib):
@@ -130,3 +141,20 @@ def test_profile_schedule_windows(lib):
     for bad in [(3, 3), (4, 2), (-1, None)]:
         with pytest.raises(ValueError):
             ProfileSchedule(*bad)
+
+
+def test_host_io_output_chunks(lib):
+    """A host-I/O captured step copies its outputs back in chunks of half the
+    layers left: the chunks tile the layers in order, the last one is a
+    single layer, and every chunk is at most as long as the layers after it
+    plus one (so its copy has attention to hide behind)."""
+    from dynamic_sparse_kv_gb300 import CapturedStep
+    assert CapturedStep.output_chunks(28) == [13, 20, 23, 25, 26, 27]
+    assert CapturedStep.output_chunks(1) == [0]
+    for L in range(1, 70):
+        ends = CapturedStep.output_chunks(L)
+        assert ends[-1] == L - 1 and all(a < b for a, b in zip(ends, ends[1:]))
+        starts = [0] + [e + 1 for e in ends[:-1]]
+        assert ends[-1] - starts[-1] == 0
+        for a, e in zip(starts, ends):
+            assert (e - a + 1) <= (L - 1 - e) + 1

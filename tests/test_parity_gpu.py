@@ -258,6 +258,43 @@ def test_fixed_adjacent_focal_layers_and_graph(focal):
     assert dec.device_status() == 0
 
 
+@pytest.mark.parametrize("kind", ["fastocr", "dense"])
+def test_host_io_graph(kind):
+    """A CapturedStep that copies its queries in from pinned host memory and
+    its outputs back inside the graph (per-layer copies on two side streams,
+    overlapped with the layers) gives the device-buffer graph's outputs and
+    selections bit for bit from the same starting selections, and re-reads
+    its host queries at every replay."""
+    from dynamic_sparse_kv_gb300 import CapturedStep
+    case = _case("qwen7b_b1", batch=2, layers=6, prompt=24, grid=(1, 12, 16), steps=10,
+                 tau=0.1, warmup=0, focal_layers=(1, 2, 4))
+    wl = case.wl
+    run = CudaDecodeRun(case).run(0, wl.steps)
+    dec = run.dec
+    cap = CapturedStep(dec, kind)
+    io = CapturedStep(dec, kind, host_io=True)
+    assert io.q_host.is_pinned() and io.out_host.is_pinned()
+    ptrs = {l: (i.data_ptr(), k.data_ptr()) for l, (i, k) in dec.sel.items()}
+    for t in (wl.steps - 1, wl.steps - 2):
+        snap = dec.state_dict()
+        dec.set_seq_len(wl.seq_len_at(t))
+        cap.q.copy_(case.q_at(t))
+        cap.replay()
+        torch.cuda.synchronize()
+        want = cap.out.cpu()
+        want_sel = {l: (i.cpu(), k.cpu()) for l, (i, k) in dec.sel.items()}
+        dec.load_state_dict(snap)   # same focal set: the graphs' buffers stay
+        assert {l: (i.data_ptr(), k.data_ptr()) for l, (i, k) in dec.sel.items()} == ptrs
+        io.out_host.fill_(-1.0)
+        io.q_host.copy_(case.q_at(t))
+        io.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(io.out_host, want), t
+        for l, (i, k) in dec.sel.items():
+            assert torch.equal(k.cpu(), want_sel[l][1]) and torch.equal(i.cpu(), want_sel[l][0]), l
+    assert dec.device_status() == 0
+
+
 def test_checkpoint_resume():
     """The method's state saved mid-warm-up and again in the steady decode and
     loaded into fresh decoders: the resumed decode gives the same outputs and
@@ -578,6 +615,33 @@ def test_read_probe_reads_every_word():
         times[n] = s.elapsed_time(e)
     assert times[1 << 30] > 2.0 * times[1 << 28]   # 4x the bytes takes well over 2x the time
     assert (1 << 30) / (times[1 << 30] * 1e-3) < 20e12   # below any plausible HBM rate
+
+
+def test_sm_copy_exact_and_refuses_pageable_memory():
+    """fastocr_copy moves bytes exactly between device memory and page-locked
+    host memory in every direction (sizes with a ragged grid-stride tail,
+    interior pointers of an allocation), and refuses pageable host memory,
+    which the device cannot address, before launching anything."""
+    from dynamic_sparse_kv_gb300 import _native as N
+    g = torch.Generator().manual_seed(5)
+    for n in (16, 4096 + 48, 3 * (1 << 20) + 16 * 777):
+        src_h = torch.randint(0, 256, (n + 64,), dtype=torch.uint8, generator=g).pin_memory()
+        dst_h = torch.zeros(n + 64, dtype=torch.uint8).pin_memory()
+        d1 = torch.zeros(n + 64, dtype=torch.uint8, device="cuda")
+        d2 = torch.zeros(n + 64, dtype=torch.uint8, device="cuda")
+        N.fastocr_copy(d1[16:], src_h[32:], n)      # host -> device
+        N.fastocr_copy(d2[48:], d1[16:], n)         # device -> device
+        N.fastocr_copy(dst_h[16:], d2[48:], n)      # device -> host
+        torch.cuda.synchronize()
+        assert torch.equal(d1[16:16 + n].cpu(), src_h[32:32 + n])
+        assert torch.equal(dst_h[16:16 + n], src_h[32:32 + n])
+        assert int(dst_h[:16].sum()) == 0 and int(dst_h[16 + n:].sum()) == 0
+    pageable = np.zeros(4096, dtype=np.uint8)
+    addr = (pageable.ctypes.data + 15) // 16 * 16
+    d = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    assert N.lib.fastocr_copy(d.data_ptr(), addr, 1024, None) == N.FASTOCR_ERR_INVALID
+    assert N.lib.fastocr_copy(addr, d.data_ptr(), 1024, None) == N.FASTOCR_ERR_INVALID
+    torch.cuda.synchronize()
 
 
 def test_length_hint_changes_speed_not_results():
