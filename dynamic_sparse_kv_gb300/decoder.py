@@ -364,18 +364,23 @@ class CapturedStep:
     the outputs once the stream reaches the replay's end. The queries come in
     through fastocr_copy, a kernel in the step's chain of programmatic
     dependent launches (the first layer stages its K/V while it runs; a copy
-    node would leave a launch gap before the first layer); the outputs go
-    out on a copy engine of a second stream in chunks of L/2, L/4, … layers
-    (the last chunk one layer), each started when its last layer's calls are
-    done, so only the input copy and the last layer's output copy are not
-    hidden behind attention. (Per-layer input copies, waited for by the
-    layers that read them, measured slower: every cross-stream wait before a
-    kernel costs the step more than the copy it hides.)
+    node there would leave a launch gap before the first layer). When the
+    queries past the first SIDE_SPLIT layers hold at least side_copy_bytes
+    (default 2 MB: at the ~170 GB/s of a host link that copy outlasts the
+    7-10 us that a cross-stream wait before a kernel costs), those go in on a
+    copy engine of a side stream instead, waited for by layer SIDE_SPLIT
+    only. The outputs go out on a copy engine of another stream in chunks of
+    L/2, L/4, ... layers (the last chunk one layer), each started when its
+    last layer's calls are done.
     """
 
+    SIDE_SPLIT = 4
+
     def __init__(self, dec: DecodeAttention, kind: str = "fastocr", fn=None,
-                 launches: int | None = None, host_io: bool = False):
+                 launches: int | None = None, host_io: bool = False,
+                 side_copy_bytes: int = 2 << 20):
         self.dec, self.kind = dec, kind
+        self.side_copy_bytes = int(side_copy_bytes)
         shape = (dec.layers, dec.batch, dec.q_heads, dec.head_dim)
         self.q = torch.zeros(shape, dtype=dec.k_cache.dtype, device=dec.k_cache.device)
         self.out = torch.zeros_like(self.q)
@@ -398,7 +403,7 @@ class CapturedStep:
         torch.cuda.current_stream().wait_stream(side)
         self.graph = torch.cuda.CUDAGraph()
         if host_io:
-            self._copy_out = torch.cuda.Stream()
+            self._copy_in, self._copy_out = torch.cuda.Stream(), torch.cuda.Stream()
         with torch.cuda.graph(self.graph):
             if host_io:
                 self._issue_with_host_io(fn)
@@ -419,14 +424,30 @@ class CapturedStep:
 
     def _issue_with_host_io(self, fn):
         main = torch.cuda.current_stream()
-        s_out = self._copy_out
+        s_in, s_out = self._copy_in, self._copy_out
+        L = self.q.shape[0]
+        per = self.q[0].numel() * self.q.element_size()
+        k = min(self.SIDE_SPLIT, L)
+        rest = None
+        if (L - k) * per >= max(self.side_copy_bytes, 1):
+            N.fastocr_copy(self.q[:k], self.q_host[:k], k * per)
+            s_in.wait_stream(main)
+            with torch.cuda.stream(s_in):
+                self.q[k:].copy_(self.q_host[k:], non_blocking=True)
+                rest = torch.cuda.Event()
+                rest.record(s_in)
+        else:
+            N.fastocr_copy(self.q, self.q_host, L * per)
         s_out.wait_stream(main)
-        N.fastocr_copy(self.q, self.q_host, self.q.numel() * self.q.element_size())
-        ends = set(self.output_chunks(self.q.shape[0]))
+        ends = set(self.output_chunks(L))
         done, first = [], [0]
 
         def hook(l, before):
-            if before or l not in ends:
+            if before:
+                if rest is not None and l == k:
+                    main.wait_event(rest)
+                return
+            if l not in ends:
                 return
             ev = torch.cuda.Event()
             ev.record(main)
@@ -438,8 +459,10 @@ class CapturedStep:
             first[0] = l + 1
 
         fn(self.q, self.out, hook=hook)
+        if rest is not None:
+            main.wait_stream(s_in)
         main.wait_stream(s_out)
-        self._events = done   # alive as long as the graph
+        self._events = done + ([rest] if rest is not None else [])   # alive with the graph
 
     def replay(self):
         self.graph.replay()

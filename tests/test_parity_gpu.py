@@ -258,13 +258,14 @@ def test_fixed_adjacent_focal_layers_and_graph(focal):
     assert dec.device_status() == 0
 
 
-@pytest.mark.parametrize("kind", ["fastocr", "dense"])
-def test_host_io_graph(kind):
+@pytest.mark.parametrize("kind,side", [("fastocr", None), ("fastocr", 0), ("dense", 0)])
+def test_host_io_graph(kind, side):
     """A CapturedStep that copies its queries in from pinned host memory and
-    its outputs back inside the graph (per-layer copies on two side streams,
-    overlapped with the layers) gives the device-buffer graph's outputs and
-    selections bit for bit from the same starting selections, and re-reads
-    its host queries at every replay."""
+    its outputs back inside the graph (queries by the SM copy kernel, with or
+    without the later layers' share on a side stream; outputs in chunks on
+    another stream, overlapped with the layers) gives the device-buffer
+    graph's outputs and selections bit for bit from the same starting
+    selections, and re-reads its host queries at every replay."""
     from dynamic_sparse_kv_gb300 import CapturedStep
     case = _case("qwen7b_b1", batch=2, layers=6, prompt=24, grid=(1, 12, 16), steps=10,
                  tau=0.1, warmup=0, focal_layers=(1, 2, 4))
@@ -272,7 +273,8 @@ def test_host_io_graph(kind):
     run = CudaDecodeRun(case).run(0, wl.steps)
     dec = run.dec
     cap = CapturedStep(dec, kind)
-    io = CapturedStep(dec, kind, host_io=True)
+    io = (CapturedStep(dec, kind, host_io=True) if side is None
+          else CapturedStep(dec, kind, host_io=True, side_copy_bytes=side))
     assert io.q_host.is_pinned() and io.out_host.is_pinned()
     ptrs = {l: (i.data_ptr(), k.data_ptr()) for l, (i, k) in dec.sel.items()}
     for t in (wl.steps - 1, wl.steps - 2):
