@@ -297,6 +297,35 @@ def test_host_io_graph(kind, side):
     assert dec.device_status() == 0
 
 
+def test_host_io_graph_rswa():
+    """The host-I/O captured R-SWA step (queries split between the SM copy
+    and the side copy engine) gives the device-buffer graph's outputs bit for
+    bit, and both match the oracle."""
+    from dynamic_sparse_kv_gb300 import CapturedStep
+    wl = synth.workload("rswa_b16", batch=3, layers=6, rswa_prefix=100, prompt=100,
+                        rswa_window=16, steps=40)
+    case = synth.make_case(wl, device="cuda")
+    dec = CudaDecodeRun(case).run(0, 2, kind="rswa").dec
+    cap = CapturedStep(dec, "rswa")
+    io = CapturedStep(dec, "rswa", host_io=True, side_copy_bytes=0)
+    kv = KVCache(case)
+    for t in (wl.steps - 1, 20):
+        dec.set_seq_len(wl.seq_len_at(t))
+        cap.q.copy_(case.q_at(t))
+        cap.replay()
+        io.q_host.copy_(case.q_at(t))
+        io.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(io.out_host, cap.out.cpu()), t
+        for l in (0, wl.layers - 1):
+            for b in range(wl.batch):
+                K, V = kv(l, b)
+                ref = A.rswa_attend(np64(case.q_at(t)[l, b]), K, V, wl.seq_len_at(t),
+                                    wl.rswa_prefix, wl.rswa_window)
+                assert_close(io.out_host[l, b], ref, TOL["bf16"], f"t={t} l={l} b={b}")
+    assert dec.device_status() == 0
+
+
 def test_checkpoint_resume():
     """The method's state saved mid-warm-up and again in the steady decode and
     loaded into fresh decoders: the resumed decode gives the same outputs and
@@ -617,6 +646,57 @@ def test_read_probe_reads_every_word():
         times[n] = s.elapsed_time(e)
     assert times[1 << 30] > 2.0 * times[1 << 28]   # 4x the bytes takes well over 2x the time
     assert (1 << 30) / (times[1 << 30] * 1e-3) < 20e12   # below any plausible HBM rate
+
+
+def test_cache_offsets_beyond_4gb():
+    """One layer whose K and V caches hold 5 GiB each (327,680 pages of 4 KV
+    heads x 16 tokens x 128 dims, bf16): a sequence on the last pages (row
+    offsets past 4 GiB) and one whose pages alternate between both ends give
+    the oracle's outputs and selection in the full, focal and gather calls."""
+    from dynamic_sparse_kv_gb300 import DecodeAttention
+    from dynamic_sparse_kv_gb300 import _native as N
+    H_q, H_kv, d, ps, num_pages = 28, 4, 128, 16, 327680
+    B, P, n_img, tau = 2, 24, 320, 0.1
+    n_t = P + n_img + 37
+    npg = (n_t + ps - 1) // ps
+    bt = torch.zeros(B, npg, dtype=torch.int32)
+    bt[0] = torch.arange(num_pages - npg, num_pages, dtype=torch.int32)
+    for i in range(npg):
+        bt[1, i] = 101 * i if i % 2 == 0 else num_pages - 1 - npg - 211 * i
+    assert int(bt.max()) * H_kv * ps * d * 2 >= 4 << 30 and int(bt[1].min()) == 0
+    k_cache = torch.empty(1, num_pages, H_kv, ps, d, dtype=torch.bfloat16, device="cuda")
+    v_cache = torch.empty_like(k_cache)
+    used = torch.unique(bt.flatten()).long().cuda()
+    g = torch.Generator(device="cuda").manual_seed(41)
+    k_cache[0, used] = torch.randn(used.numel(), H_kv, ps, d, generator=g, device="cuda").bfloat16()
+    v_cache[0, used] = torch.randn(used.numel(), H_kv, ps, d, generator=g, device="cuda").bfloat16()
+    q = (2.0 * torch.randn(B, H_q, d, generator=g, device="cuda")).bfloat16()
+    img = torch.tensor([[P, n_img]] * B, dtype=torch.int32, device="cuda")
+    dec = DecodeAttention(k_cache, v_cache, bt.cuda(), q_heads=H_q, img_range=img,
+                          max_img=n_img, tau=tau)
+    dec.set_seq_len(n_t)
+    out_f, out_c, out_s = (torch.empty_like(q) for _ in range(3))
+    idx = torch.zeros(B, dec.stride, dtype=torch.int32, device="cuda")
+    k = torch.zeros(B, dtype=torch.int32, device="cuda")
+    N.fastocr_full_attend(dec.handle, q, dec.kv[0], out_f)
+    N.fastocr_focal_attend(dec.handle, q, dec.kv[0], img, tau, out_c, idx, dec.stride, k)
+    N.fastocr_sparse_attend(dec.handle, q, dec.kv[0], img, idx, dec.stride, k, out_s)
+    torch.cuda.synchronize()
+    assert dec.device_status() == 0
+    for b in range(B):
+        pages = k_cache[0, bt[b].long().cuda()]
+        K = np64(pages.permute(0, 2, 1, 3).reshape(npg * ps, H_kv, d)[:n_t])
+        pages = v_cache[0, bt[b].long().cuda()]
+        V = np64(pages.permute(0, 2, 1, 3).reshape(npg * ps, H_kv, d)[:n_t])
+        qb = np64(q[b])
+        assert_close(out_f[b], A.full_attend(qb, K, V, n_t), TOL["bf16"], f"full b={b}")
+        ref, sel, sigma = A.focal_attend(qb, K, V, n_t, P, n_img, tau)
+        assert_close(out_c[b], ref, TOL["bf16"], f"focal b={b}")
+        got = idx[b, :int(k[b])].cpu().numpy()
+        check_selection(got, sel, sigma, P, f"selection b={b}")
+        assert_close(out_s[b], A.sparse_attend(qb, K, V, n_t, P, n_img, got), TOL["bf16"],
+                     f"gather b={b}")
+    dec.close()
 
 
 def test_sm_copy_exact_and_refuses_pageable_memory():
