@@ -429,7 +429,7 @@ class CapturedStep:
         per = self.q[0].numel() * self.q.element_size()
         k = min(self.SIDE_SPLIT, L)
         rest = None
-        if (L - k) * per >= max(self.side_copy_bytes, 1):
+        if k < L and (L - k) * per >= self.side_copy_bytes:   # 0 forces the side copy
             N.fastocr_copy(self.q[:k], self.q_host[:k], k * per)
             s_in.wait_stream(main)
             with torch.cuda.stream(s_in):
