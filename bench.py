@@ -387,7 +387,7 @@ class Bench:
                 dec.begin_warmup()
                 for t in range(wl.warmup):   # the method's profiling warm-up (untimed)
                     dec.set_seq_len(wl.seq_len_at(t))
-                    dec.warmup_step(case.q_at(t).contiguous(), qw)
+                    dec.warmup_step(case.q_at(t).contiguous(), qw, select=t == wl.warmup - 1)
                 focal, _ = dec.finish_warmup(wl.n_focal)
         dec.set_seq_len(self.wl.seq_len_at(self.t_of(0)))
         return dec, focal, CapturedStep(dec, kind)
@@ -632,7 +632,11 @@ class Bench:
         dec1.close()
         pcap = CapturedStep(dec, "profile")
         ms, _, _, _ = self.time_graph(dec, pcap, 0.5)
-        compare["profile_us_per_step"] = ms * 1e3 / self.args.steps
+        compare["profile_us_per_step"] = ms * 1e3 / self.args.steps   # a window's last step
+        del pcap
+        pcap = CapturedStep(dec, "profile_mass")
+        ms, _, _, _ = self.time_graph(dec, pcap, 0.5)
+        compare["profile_mass_us_per_step"] = ms * 1e3 / self.args.steps   # its earlier steps
         torch.cuda.synchronize()
         c0 = time.perf_counter()
         del pcap

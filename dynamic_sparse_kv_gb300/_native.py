@@ -64,6 +64,7 @@ def _load() -> ctypes.CDLL:
         "fastocr_focal_attend": ([P, P, ctypes.POINTER(fastocr_kv), P, F64, P, P, I32, P, I32, P],
                                  I32),
         "fastocr_focal_scores": ([P, P, ctypes.POINTER(fastocr_kv), P, P, P, I32, P], I32),
+        "fastocr_profile_attend": ([P, P, ctypes.POINTER(fastocr_kv), P, P, I32, P], I32),
         "fastocr_select": ([P, ctypes.POINTER(fastocr_kv), P, P, I32, F64, P, I32, P, P], I32),
         "fastocr_sparse_attend": ([P, P, ctypes.POINTER(fastocr_kv), P, P, I32, P, P, P], I32),
         "fastocr_sparse_attend_ex": ([P, P, ctypes.POINTER(fastocr_kv), P, P, I32, P, P,
@@ -151,6 +152,14 @@ def fastocr_focal_attend(handle, q, kv: fastocr_kv, img_range, tau, out, idx, id
            lib.fastocr_focal_attend(handle, _ptr(q), ctypes.byref(kv), _ptr(img_range),
                                     float(tau), _ptr(out), _ptr(idx), int(idx_stride),
                                     _ptr(k_out), int(profile_layer), _stream(stream)))
+
+
+def fastocr_profile_attend(handle, q, kv: fastocr_kv, img_range, out, profile_layer,
+                           stream=None) -> None:
+    """Full attention that adds the layer's image mass to the profiler; no selection."""
+    _check("fastocr_profile_attend",
+           lib.fastocr_profile_attend(handle, _ptr(q), ctypes.byref(kv), _ptr(img_range),
+                                      _ptr(out), int(profile_layer), _stream(stream)))
 
 
 def fastocr_focal_scores(handle, q, kv: fastocr_kv, img_range, out, sigma, sigma_stride,

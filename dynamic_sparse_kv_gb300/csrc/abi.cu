@@ -264,6 +264,20 @@ fastocr_status fastocr_focal_attend(fastocr_handle* h, const void* q, const fast
   return launch(h, kFocal, expected_tokens(h), p, stream);
 }
 
+fastocr_status fastocr_profile_attend(fastocr_handle* h, const void* q, const fastocr_kv* kv,
+                                      const int32_t* img_range, void* out, int32_t profile_layer,
+                                      fastocr_stream stream) {
+  if (!h || !q || !out || !img_range) return FASTOCR_ERR_NULL;
+  fastocr_status st = check_kv(h, kv);
+  if (st != FASTOCR_OK) return st;
+  if (!aligned16(q) || !aligned16(out)) return FASTOCR_ERR_ALIGN;
+  if (profile_layer < 0 || profile_layer >= h->dims.num_layers) return FASTOCR_ERR_INVALID;
+  Params p = base_params(h, q, kv, out);
+  p.img_range = img_range;
+  p.profile_layer = profile_layer;
+  return launch(h, kProfile, expected_tokens(h), p, stream);
+}
+
 fastocr_status fastocr_focal_scores(fastocr_handle* h, const void* q, const fastocr_kv* kv,
                                     const int32_t* img_range, void* out, float* sigma,
                                     int32_t sigma_stride, fastocr_stream stream) {

@@ -293,7 +293,7 @@ __device__ __forceinline__ CtaList make_cta_list(const Params& p, int b, int spl
   const int cur = n_t - 1;
   int a1 = 0, len1 = 0, a2 = 0, len2 = 0, in_set = 0;
   if (n_t >= 1) {
-    if (MODE == kFull || MODE == kFocal) {
+    if (MODE == kFull || MODE == kFocal || MODE == kProfile) {
       len1 = n_t - 1;
       in_set = 1;
     } else if (MODE == kRswa) {
@@ -729,6 +729,7 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
       for (int e = 0; e < 4; ++e) sm_.acc[mt][e] = 0.f;
     sm_.m[0] = sm_.m[1] = kNegInf;
     sm_.l[0] = sm_.l[1] = 0.f;
+    sm_.il[0] = sm_.il[1] = 0.f;
   } else {
     float* qs = reinterpret_cast<float*>(smem + SM::kQOffset);
     for (int e = tid; e < kSlots * D; e += kThreads) {
@@ -739,6 +740,7 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
     for (int h = 0; h < kSlots; ++h) {
       sf_.m[h] = kNegInf;
       sf_.l[h] = 0.f;
+      sf_.il[h] = 0.f;
 #pragma unroll
       for (int j = 0; j < D / 32; ++j) sf_.acc[h][j] = 0.f;
     }
@@ -818,6 +820,10 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
       const float al1 = fast_exp2(sm_.m[1] - (mn1 == kNegInf ? 0.f : mn1));
       sm_.l[0] *= al0;
       sm_.l[1] *= al1;
+      if constexpr (MODE == kProfile) {
+        sm_.il[0] *= al0;
+        sm_.il[1] *= al1;
+      }
       sm_.m[0] = mn0;
       sm_.m[1] = mn1;
 #pragma unroll
@@ -837,11 +843,18 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
     // that multiply V sum to exactly 1 after normalisation (rounding moves a
     // weight by at most 2^-9 relative, never the total). A focal layer's sum
     // also turns its logits into the image scores, which must be the
-    // probabilities themselves, so there it adds the unrounded values.
+    // probabilities themselves, so there it adds the unrounded values; so does
+    // a profiling layer, whose image mass is a ratio of such sums.
     const uint32_t pk01 = pack_bf16(p0, p1), pk23 = pack_bf16(p2, p3);
-    if (MODE == kFocal) {
+    if (MODE == kFocal || MODE == kProfile) {
       sm_.l[0] += p0 + p2;
       sm_.l[1] += p1 + p3;
+      if constexpr (MODE == kProfile) {
+        const bool iA = posA >= c.img_start && posA < c.img_start + c.n_img;
+        const bool iB = posB >= c.img_start && posB < c.img_start + c.n_img;
+        sm_.il[0] += (iA ? p0 : 0.f) + (iB ? p2 : 0.f);
+        sm_.il[1] += (iA ? p1 : 0.f) + (iB ? p3 : 0.f);
+      }
     } else {
       sm_.l[0] += __uint_as_float(pk01 << 16) + __uint_as_float(pk23 << 16);
       sm_.l[1] += __uint_as_float(pk01 & 0xffff0000u) + __uint_as_float(pk23 & 0xffff0000u);
@@ -962,6 +975,9 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
           const float al = fast_exp2(sf_.m[h] - base);
           pr[h] = fast_exp2(s[h] - base);
           sf_.l[h] = sf_.l[h] * al + (half == 0 ? pr[h] : 0.f);
+          if constexpr (MODE == kProfile)
+            sf_.il[h] = sf_.il[h] * al +
+                        (half == 0 && pos >= c.img_start && pos < c.img_start + c.n_img ? pr[h] : 0.f);
           sf_.m[h] = mn;
 #pragma unroll
           for (int j = 0; j < D / 32; ++j) sf_.acc[h][j] *= al;
@@ -996,6 +1012,7 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
   float* wm = reinterpret_cast<float*>(smem + E::kWm);
   float* wl = reinterpret_cast<float*>(smem + E::kWl);
   float* wacc = reinterpret_cast<float*>(smem + E::kWacc);
+  float* wil = reinterpret_cast<float*>(smem + E::kWil);   // profile mode
   if constexpr (kMma) {
     const float l0 = warp_sum_gid(sm_.l[0]), l1 = warp_sum_gid(sm_.l[1]);
     const int h0 = warp * kSlots + 2 * tig, h1 = h0 + 1;
@@ -1004,6 +1021,13 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
       wm[h1] = sm_.m[1];
       wl[h0] = l0;
       wl[h1] = l1;
+    }
+    if constexpr (MODE == kProfile) {
+      const float il0 = warp_sum_gid(sm_.il[0]), il1 = warp_sum_gid(sm_.il[1]);
+      if (gid == 0) {
+        wil[h0] = il0;
+        wil[h1] = il1;
+      }
     }
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) {
@@ -1021,6 +1045,12 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
       if (lane == 0) {
         wm[warp * kSlots + h] = sf_.m[h];
         wl[warp * kSlots + h] = l;
+      }
+      if constexpr (MODE == kProfile) {
+        float il = sf_.il[h];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) il += __shfl_xor_sync(0xffffffffu, il, o);
+        if (lane == 0) wil[warp * kSlots + h] = il;
       }
 #pragma unroll
       for (int j = 0; j < D / 32; ++j) wacc[(warp * kSlots + h) * D + lane + 32 * j] = sf_.acc[h][j];
@@ -1103,6 +1133,27 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
       for (int w = 0; w < kWarps; ++w) L = fmaf(wl[w * kSlots + tid], sc[w], L);
       sM[tid] = M == kNegInf ? 0.f : M;
       sInvL[tid] = L > 0.f ? __frcp_rn(L) : 0.f;
+    }
+    if constexpr (MODE == kProfile) {
+      // the unit's image mass: sum over its heads of (image share of the
+      // softmax sum) / (softmax sum), added to the layer's profiler slot
+      if (warp == 0) {
+        double mass = 0.0;
+        if (lane < p.g) {
+          float sc[kWarps];
+          warp_scales(lane, sc);
+          float L = 0.f, IL = 0.f;
+#pragma unroll
+          for (int w = 0; w < kWarps; ++w) {
+            L = fmaf(wl[w * kSlots + lane], sc[w], L);
+            IL = fmaf(wil[w * kSlots + lane], sc[w], IL);
+          }
+          mass = L > 0.f ? (double)IL / (double)L : 0.0;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mass += __shfl_xor_sync(0xffffffffu, mass, o);
+        if (lane == 0) atomicAdd(p.profile + p.profile_layer, mass);
+      }
     }
   } else {
     // ---------------- push the CTA partial to the CTAs of the cluster
@@ -1194,6 +1245,27 @@ __global__ void __launch_bounds__(32 * warps_for(V), ctas_per_sm(V)) attend_kern
       if (ok && sub == 0) store_pair(e, acc);
     }
     if (MODE == kFocal && tid < kSlots) head_stats(tid, sM[tid], sInvL[tid]);
+    if constexpr (MODE == kProfile) {
+      // this CTA's share of the unit's image mass: its image sums rescaled to
+      // the heads' max over the cluster, over the heads' sum over the cluster
+      // (the S shares add up to the unit's mass in the profiler slot)
+      if (warp == 0) {
+        double mass = 0.0;
+        if (lane < p.g) {
+          float base, inv, sc[kWarps];
+          head_stats(lane, base, inv);
+          const float Mc = warp_scales(lane, sc);
+          float IL = 0.f;
+#pragma unroll
+          for (int w = 0; w < kWarps; ++w) IL = fmaf(wil[w * kSlots + lane], sc[w], IL);
+          const float bc = Mc == kNegInf ? 0.f : Mc;
+          mass = IL > 0.f ? (double)(IL * fast_exp2(bc - base)) * (double)inv : 0.0;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mass += __shfl_xor_sync(0xffffffffu, mass, o);
+        if (lane == 0) atomicAdd(p.profile + p.profile_layer, mass);
+      }
+    }
   }
 
   // ---------------- focal: scores of the image tokens this CTA streamed
@@ -1297,6 +1369,7 @@ cudaError_t prepare_modes() {
   if ((e = prepare_attend(attend_kernel<T, D, kFull, V>, bytes))) return e;
   if ((e = prepare_attend(attend_kernel<T, D, kFocal, V>, bytes))) return e;
   if ((e = prepare_attend(attend_kernel<T, D, kSparse, V>, bytes))) return e;
+  if ((e = prepare_attend(attend_kernel<T, D, kProfile, V>, bytes))) return e;
   return prepare_attend(attend_kernel<T, D, kRswa, V>, bytes);
 }
 
@@ -1382,6 +1455,7 @@ cudaError_t dispatch_variant(int mode, const Params& p, cudaStream_t s) {
     case kFocal: return launch_attend<T, D, kFocal, V>(p, s);
     case kSparse: return launch_attend<T, D, kSparse, V>(p, s);
     case kRswa: return launch_attend<T, D, kRswa, V>(p, s);
+    case kProfile: return launch_attend<T, D, kProfile, V>(p, s);
   }
   return cudaErrorInvalidValue;
 }

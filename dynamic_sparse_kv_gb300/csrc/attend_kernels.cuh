@@ -52,7 +52,10 @@ constexpr float kLazyMax = 8.f; // running-max slack (log2 units) before a resca
 constexpr int kMaxSplits = 16;  // = the largest thread-block cluster used
 constexpr int kMaxImg = 16384; // image tokens whose scores fit in shared memory
 
-enum Mode : int { kFull = 0, kFocal = 1, kSparse = 2, kRswa = 3 };
+// kProfile: full attention that also adds the layer's image-attention mass
+// to the profiler (a warm-up step whose selections are not kept): no logits,
+// no scores, no selection kernel.
+enum Mode : int { kFull = 0, kFocal = 1, kSparse = 2, kRswa = 3, kProfile = 4 };
 
 // device status bits (same values as FASTOCR_DEV_* in fastocr.h)
 constexpr int kDevBadPage = 1;
@@ -249,7 +252,7 @@ __device__ __forceinline__ AttendList make_list(const Params& p, int b, int& bad
   L.tail_start = 0;
   L.img_start = 0;
   L.n_img = 0;
-  if (MODE == kFocal || MODE == kSparse) {
+  if (MODE == kFocal || MODE == kSparse || MODE == kProfile) {
     int s = __ldcg(p.img_range + 2 * b), n = __ldcg(p.img_range + 2 * b + 1);
     if (s < 0 || n < 0 || s > n_t || n > n_t - s || (MODE == kFocal && n > p.max_img)) {
       bad |= kDevBadImg;
@@ -295,13 +298,15 @@ struct Smem {
 template <int D, int kWarps>
 struct EpiSmem {
   // reuses the pipeline area once streaming is done: per-warp partials
-  // wm[W][8], wl[W][8], wacc[W][8][D]; focal: the heads' max M[8], 1/sum invL[8]
+  // wm[W][8], wl[W][8], wacc[W][8][D]; focal: the heads' max M[8], 1/sum invL[8];
+  // profile: the per-warp image sums wil[W][8]
   static constexpr int kWm = 0;
   static constexpr int kWl = kWm + kWarps * kSlots * 4;
   static constexpr int kWacc = kWl + kWarps * kSlots * 4;
   static constexpr int kM = kWacc + kWarps * kSlots * D * 4;
   static constexpr int kInvL = kM + kSlots * 4;
-  static constexpr int kBytes = kInvL + kSlots * 4;
+  static constexpr int kWil = kInvL + kSlots * 4;
+  static constexpr int kBytes = kWil + kWarps * kSlots * 4;
 };
 
 template <typename T, int D, int V = kGeneral>
@@ -383,6 +388,7 @@ template <int D>
 struct WarpStateMma {
   float acc[D / 16][4];
   float m[2], l[2];
+  float il[2];   // profile mode: the image tokens' share of l
   uint32_t qf[D / 16][2];
 };
 
@@ -391,6 +397,7 @@ template <int D>
 struct WarpStateF32 {
   float acc[kSlots][D / 32];
   float m[kSlots], l[kSlots];
+  float il[kSlots];   // profile mode: the image tokens' share of l
 };
 
 }  // namespace fastocr

@@ -176,15 +176,22 @@ class DecodeAttention:
         self.warm_k = torch.zeros(self.layers, self.batch, dtype=torch.int32, device=dev)
         N.fastocr_profiler_reset(self.handle, stream)
 
-    def warmup_step(self, q, out, stream=None, hook=None):
-        """Full attention in every layer, profiling image mass; keeps every layer's
-        selection so that F_last can be taken once C is known."""
+    def warmup_step(self, q, out, stream=None, hook=None, select=True):
+        """Full attention in every layer, profiling image mass. select=True (the
+        last step of a profiling window) also keeps every layer's selection,
+        so that F_last can be taken once C is known; the window's earlier
+        steps pass select=False and only profile (fastocr_profile_attend: one
+        kernel a layer, no logits, scores or top-k)."""
         for l in range(self.layers):
             if hook:
                 hook(l, True)
-            N.fastocr_focal_attend(self.handle, q[l], self.kv[l], self.img_range, self.tau,
-                                   out[l], self.warm_idx[l], self.stride, self.warm_k[l],
-                                   profile_layer=l, stream=stream)
+            if select:
+                N.fastocr_focal_attend(self.handle, q[l], self.kv[l], self.img_range, self.tau,
+                                       out[l], self.warm_idx[l], self.stride, self.warm_k[l],
+                                       profile_layer=l, stream=stream)
+            else:
+                N.fastocr_profile_attend(self.handle, q[l], self.kv[l], self.img_range, out[l],
+                                         l, stream)
             if hook:
                 hook(l, False)
 
@@ -212,8 +219,9 @@ class DecodeAttention:
             return None
         if pos == 0:
             self.begin_warmup(stream)
-        self.warmup_step(q, out, stream)
-        if pos == schedule.window - 1:
+        last = pos == schedule.window - 1
+        self.warmup_step(q, out, stream, select=last)
+        if last:
             return self.finish_warmup(n_focal, stream)[0]
         return None
 
@@ -341,7 +349,7 @@ class DecodeAttention:
             return self.layers + len(self.focal)
         if kind == "profile":
             return 2 * self.layers
-        return self.layers
+        return self.layers   # "profile_mass", "dense", "rswa": one kernel a layer
 
     def device_status(self, stream=None) -> int:
         return N.fastocr_device_status(self.handle, stream)
@@ -353,8 +361,10 @@ class CapturedStep:
     q, out: [L, B, H_q, d] device tensors owned by this object; write the
     step's queries into q (and N_t into dec.seq_len), then replay(). kind:
     "fastocr" (steady FastOCR step), "dense" (full attention in every layer),
-    "profile" (a profiling step: full attention with scoring, selection and
-    profile accumulation in every layer) or "rswa"; or any name with `fn`, a
+    "profile" (the last step of a profiling window: full attention with
+    scoring, selection and profile accumulation in every layer),
+    "profile_mass" (an earlier step of the window: full attention and
+    profile accumulation only) or "rswa"; or any name with `fn`, a
     callable fn(q, out, stream) that issues the calls (e.g. a subset of the
     step's layers), and `launches`, the kernels it launches.
 
@@ -390,11 +400,13 @@ class CapturedStep:
                 raise ValueError("host_io captures one of the step kinds, not a custom fn")
             self.q_host = torch.zeros(shape, dtype=self.q.dtype, pin_memory=True)
             self.out_host = torch.zeros(shape, dtype=self.q.dtype, pin_memory=True)
-        if kind == "profile" and dec.warm_idx is None:
+        if kind in ("profile", "profile_mass") and dec.warm_idx is None:
             dec.begin_warmup()
         if fn is None:   # otherwise fn(q, out, stream) issues the calls and `launches` counts them
             fn = {"fastocr": dec.step, "dense": dec.dense_step, "rswa": dec.rswa_step,
-                  "profile": dec.warmup_step}[kind]
+                  "profile": dec.warmup_step,
+                  "profile_mass": lambda q, out, stream=None, hook=None:
+                      dec.warmup_step(q, out, stream, hook, select=False)}[kind]
             launches = dec.launches_per_step(kind)
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())

@@ -81,9 +81,9 @@ extern "C" {
 #endif
 
 /* 2 adds fastocr_focal_scores, fastocr_select, fastocr_set_variant,
- * fastocr_read_probe, fastocr_copy, fastocr_profiler_read /
- * fastocr_profiler_load and fastocr_sparse_attend_ex to version 1; no call
- * of version 1 changed. */
+ * fastocr_read_probe, fastocr_copy, fastocr_profile_attend,
+ * fastocr_profiler_read / fastocr_profiler_load and fastocr_sparse_attend_ex
+ * to version 1; no call of version 1 changed. */
 #define FASTOCR_ABI_VERSION 2
 
 typedef struct fastocr_handle fastocr_handle;
@@ -167,6 +167,23 @@ fastocr_status fastocr_focal_attend(fastocr_handle* h, const void* q, const fast
                                     const int32_t* img_range, double tau, void* out,
                                     int32_t* idx, int32_t idx_stride, int32_t* k_out,
                                     int32_t profile_layer, fastocr_stream stream);
+
+/* Focal-layer profiling without a selection [FGP, focal layer selection]:
+ * full decode attention over [0, N_t) (out as fastocr_full_attend), and the
+ * image probability mass -- for every sequence and query head, the softmax
+ * probability of the layer's full-cache attention summed over the image
+ * tokens [start_b, start_b + N_img_b) -- summed into profiler slot
+ * profile_layer (0 <= profile_layer < num_layers), the quantity
+ * fastocr_focal_attend adds with profile_layer >= 0. One kernel: no image
+ * logits, scores or top-k are made. For the warm-up steps whose selections
+ * nothing reads (every step of a profiling window but its last, whose
+ * selection of the deepest chosen layer becomes F_last). The mass is summed
+ * per (sequence, KV head) group and split in double-precision atomics, so
+ * its last bits depend on their order; img_range as fastocr_focal_attend
+ * (max_img_tokens does not bound it). */
+fastocr_status fastocr_profile_attend(fastocr_handle* h, const void* q, const fastocr_kv* kv,
+                                      const int32_t* img_range, void* out, int32_t profile_layer,
+                                      fastocr_stream stream);
 
 /* Head-sharded focal layer, part 1 [FGP]: what fastocr_focal_attend computes
  * for this handle's heads, without the selection. A sequence's heads may be

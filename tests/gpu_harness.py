@@ -146,8 +146,10 @@ class CudaDecodeRun:
                 dec.rswa_step(q, out)
             elif self.schedule.position(t) >= 0 and self.focal_fixed is None:
                 chosen = dec.scheduled_step(t, q, out, self.schedule, wl.n_focal)
-                self.sels[t] = self._selections(
-                    {l: (dec.warm_idx[l], dec.warm_k[l]) for l in range(wl.layers)})
+                if self.schedule.position(t) == wl.warmup - 1:
+                    # only a window's last step selects (F_last comes from it)
+                    self.sels[t] = self._selections(
+                        {l: (dec.warm_idx[l], dec.warm_k[l]) for l in range(wl.layers)})
                 if chosen is not None:
                     self.focal = tuple(chosen)
                     self.focal_history.append((t, self.focal))

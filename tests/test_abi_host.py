@@ -74,6 +74,8 @@ def test_host_checks_without_gpu(lib):
     assert L.fastocr_focal_attend(None, None, ctypes.byref(kv), None, 0.5, None, None, 1, None,
                                   -1, None) == N.FASTOCR_ERR_NULL
     assert L.fastocr_profiler_select(None, 1, None, None, None) == N.FASTOCR_ERR_NULL
+    assert L.fastocr_profile_attend(None, None, ctypes.byref(kv), None, None, 0,
+                                    None) == N.FASTOCR_ERR_NULL
     assert L.fastocr_profiler_read(None, None, None) == N.FASTOCR_ERR_NULL
     assert L.fastocr_profiler_load(None, None, None) == N.FASTOCR_ERR_NULL
     assert L.fastocr_set_splits(None, 0, 1) == N.FASTOCR_ERR_NULL

@@ -89,7 +89,7 @@ def test_tau_one_equals_dense_on_gpu():
     for t in range(case.wl.steps):
         d = (run.outs[t].float() - dense.outs[t].float()).abs().max().item()
         assert d <= 2e-2, (t, d)
-        assert set(run.sels[t].keys()) <= set(range(case.wl.layers))
+        assert set(run.sels.get(t, {}).keys()) <= set(range(case.wl.layers))
 
 
 def test_rswa_small():
@@ -355,7 +355,8 @@ def test_checkpoint_resume():
     for t in range(wl.steps):
         got = (part if t < t1 else res if t < t2 else res2)
         assert torch.equal(got.outs[t], whole.outs[t]), f"step {t}"
-        for l, sel in whole.sels[t].items():
+        assert (t in got.sels) == (t in whole.sels), t   # warm-up: only a window's last step selects
+        for l, sel in whole.sels.get(t, {}).items():
             for b in range(wl.batch):
                 assert np.array_equal(got.sels[t][l][b], sel[b]), f"step {t} layer {l} seq {b}"
     compare_decode(whole, wl.steps)
@@ -880,6 +881,52 @@ def test_score_reduce_path_whole_decode():
     run.run(0, case.wl.steps)
     compare_decode(run, case.wl.steps)
     assert len(calls) == 2 * (case.wl.steps - case.wl.warmup)   # two focal layers a step
+
+
+@pytest.mark.parametrize("splits", [None, 1, 5])
+@pytest.mark.parametrize("shape", [dict(), dict(q_heads=6, kv_heads=3, head_dim=128, dtype="f32")],
+                         ids=["bf16_g7", "f32_g2"])
+def test_profile_attend_mass(shape, splits):
+    """The profile-only layer (fastocr_profile_attend, the warm-up steps that
+    keep no selection): its output is full attention, and the image mass it
+    adds to its profiler slot is the oracle's sum over sequences and query
+    heads of the image tokens' probabilities, and the mass the focal call
+    adds, to within 1e-5 relative; forced split counts merge the mass over a
+    cluster."""
+    from dynamic_sparse_kv_gb300 import DecodeAttention
+    from dynamic_sparse_kv_gb300 import _native as N
+    case = _case("qwen7b_b1", batch=3, layers=2, prompt=37, grid=(1, 24, 20), steps=40, tau=0.1,
+                 **shape)
+    wl = case.wl
+    t = 35
+    n_t = wl.seq_len_at(t)
+    dec = DecodeAttention(case.k_cache, case.v_cache, case.block_table, q_heads=wl.q_heads,
+                          img_range=case.img_range, max_img=wl.n_img, tau=wl.tau,
+                          splits={0: splits} if splits else None)
+    dec.set_seq_len(n_t)
+    dec.begin_warmup()                                # profiler slots zeroed
+    q = case.q_at(t)[0].contiguous()
+    out_p, out_f = torch.empty_like(q), torch.empty_like(q)
+    idx = torch.zeros(wl.batch, dec.stride, dtype=torch.int32, device="cuda")
+    k = torch.zeros(wl.batch, dtype=torch.int32, device="cuda")
+    N.fastocr_profile_attend(dec.handle, q, dec.kv[0], case.img_range, out_p, 0)
+    N.fastocr_profile_attend(dec.handle, q, dec.kv[0], case.img_range, out_p, 0)   # adds again
+    N.fastocr_focal_attend(dec.handle, q, dec.kv[0], case.img_range, wl.tau, out_f, idx,
+                           dec.stride, k, profile_layer=1)
+    torch.cuda.synchronize()
+    assert dec.device_status() == 0
+    mass = N.fastocr_profiler_read(dec.handle, 2)
+    kv = KVCache(case)
+    want, tol = 0.0, TOL[wl.dtype]
+    for b in range(wl.batch):
+        Kl, Vl = kv(0, b)
+        out, probs = A.attend(np64(q[b]), Kl, Vl, A.full_positions(n_t))
+        want += float(A.image_scores(probs, wl.prompt, wl.n_img).sum())
+        assert_close(out_p[b], out, tol, f"profile b={b}")
+        assert_close(out_f[b], out, tol, f"focal b={b}")
+    assert abs(mass[0] / 2 - want) <= 1e-5 * want, (mass, want)
+    assert abs(mass[1] - want) <= 1e-5 * want, (mass, want)
+    dec.close()
 
 
 @pytest.mark.parametrize("variant", list(VARIANTS))
