@@ -385,10 +385,12 @@ class Bench:
             else:
                 qw = self.torch.empty_like(case.q_at(0))
                 dec.begin_warmup()
+                q_t = None
                 for t in range(wl.warmup):   # the method's profiling warm-up (untimed)
                     dec.set_seq_len(wl.seq_len_at(t))
-                    dec.warmup_step(case.q_at(t).contiguous(), qw, select=t == wl.warmup - 1)
-                focal, _ = dec.finish_warmup(wl.n_focal)
+                    q_t = case.q_at(t).contiguous()
+                    dec.warmup_step(q_t, qw, select=False)
+                focal, _ = dec.finish_warmup(wl.n_focal, q=q_t)
         dec.set_seq_len(self.wl.seq_len_at(self.t_of(0)))
         return dec, focal, CapturedStep(dec, kind)
 
@@ -630,13 +632,11 @@ class Bench:
         compare["tau1_us_per_step"] = ms * 1e3 / self.args.steps
         del cap1
         dec1.close()
-        pcap = CapturedStep(dec, "profile")
-        ms, _, _, _ = self.time_graph(dec, pcap, 0.5)
-        compare["profile_us_per_step"] = ms * 1e3 / self.args.steps   # a window's last step
-        del pcap
+        # a profiling window's step (full attention, mass in the epilogue); the
+        # window's end adds one focal layer (config.alone.focal)
         pcap = CapturedStep(dec, "profile_mass")
         ms, _, _, _ = self.time_graph(dec, pcap, 0.5)
-        compare["profile_mass_us_per_step"] = ms * 1e3 / self.args.steps   # its earlier steps
+        compare["profile_us_per_step"] = ms * 1e3 / self.args.steps
         torch.cuda.synchronize()
         c0 = time.perf_counter()
         del pcap

@@ -177,11 +177,11 @@ class DecodeAttention:
         N.fastocr_profiler_reset(self.handle, stream)
 
     def warmup_step(self, q, out, stream=None, hook=None, select=True):
-        """Full attention in every layer, profiling image mass. select=True (the
-        last step of a profiling window) also keeps every layer's selection,
-        so that F_last can be taken once C is known; the window's earlier
-        steps pass select=False and only profile (fastocr_profile_attend: one
-        kernel a layer, no logits, scores or top-k)."""
+        """Full attention in every layer, profiling image mass. select=False
+        (what scheduled_step runs) only profiles (fastocr_profile_attend: one
+        kernel a layer, no logits, scores or top-k), and finish_warmup(q=...)
+        then selects on the deepest chosen layer alone; select=True also keeps
+        every layer's selection, for finish_warmup to take F_last from."""
         for l in range(self.layers):
             if hook:
                 hook(l, True)
@@ -195,14 +195,23 @@ class DecodeAttention:
             if hook:
                 hook(l, False)
 
-    def finish_warmup(self, n_focal: int, stream=None):
-        """Choose C from the profile; F_last = last warm-up selection of max(C)."""
+    def finish_warmup(self, n_focal: int, stream=None, q=None):
+        """Choose C from the profile; F_last = the last warm-up step's selection
+        of max(C). q: that step's queries, when it only profiled (then the
+        deepest chosen layer's selection is made now, by one focal call on
+        the same queries and cache, so the step must directly precede this
+        call); None when it selected in every layer (warmup_step(select=True))."""
         focal, mass = N.fastocr_profiler_select(self.handle, n_focal, self.layers, stream)
         self.set_focal_layers(focal)
         deepest = max(self.focal)
         idx, k = self.sel[deepest]
-        idx.copy_(self.warm_idx[deepest])
-        k.copy_(self.warm_k[deepest])
+        if q is None:
+            idx.copy_(self.warm_idx[deepest])
+            k.copy_(self.warm_k[deepest])
+        else:
+            scratch = torch.empty_like(q[deepest])   # the step's output of this layer is in out
+            N.fastocr_focal_attend(self.handle, q[deepest], self.kv[deepest], self.img_range,
+                                   self.tau, scratch, idx, self.stride, k, -1, stream)
         self.has_f_last = True
         return focal, mass
 
@@ -219,18 +228,20 @@ class DecodeAttention:
             return None
         if pos == 0:
             self.begin_warmup(stream)
-        last = pos == schedule.window - 1
-        self.warmup_step(q, out, stream, select=last)
-        if last:
-            return self.finish_warmup(n_focal, stream)[0]
+        # every step of the window only profiles; at its end the deepest
+        # chosen layer selects on the last step's queries (F_last)
+        self.warmup_step(q, out, stream, select=False)
+        if pos == schedule.window - 1:
+            return self.finish_warmup(n_focal, stream, q=q)[0]
         return None
 
     # ------------------------------------------------------------ checkpoint
     def state_dict(self, stream=None) -> dict:
         """The method's state between decode steps, on the host: the focal set
         C, the selections of the focal layers (the deepest one is F_last, the
-        next step's carried selection) and, while a warm-up window is open, its
-        per-layer selections and the profiler's accumulated image mass.
+        next step's carried selection) and, while a warm-up window is open, the
+        profiler's accumulated image mass (with the per-layer selection buffers
+        of warmup_step(select=True), which the scheduled window leaves unused).
         Synchronises the stream. The KV cache is the caller's and not part of it."""
         if stream is not None:
             stream.synchronize()

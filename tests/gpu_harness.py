@@ -146,13 +146,13 @@ class CudaDecodeRun:
                 dec.rswa_step(q, out)
             elif self.schedule.position(t) >= 0 and self.focal_fixed is None:
                 chosen = dec.scheduled_step(t, q, out, self.schedule, wl.n_focal)
-                if self.schedule.position(t) == wl.warmup - 1:
-                    # only a window's last step selects (F_last comes from it)
-                    self.sels[t] = self._selections(
-                        {l: (dec.warm_idx[l], dec.warm_k[l]) for l in range(wl.layers)})
                 if chosen is not None:
                     self.focal = tuple(chosen)
                     self.focal_history.append((t, self.focal))
+                    # a window's end selects on its last step's queries in the
+                    # deepest chosen layer only: that selection is F_last
+                    d = max(self.focal)
+                    self.sels[t] = self._selections({d: dec.sel[d]})
             else:
                 if self.focal is None:
                     self.focal = tuple(self.focal_fixed)

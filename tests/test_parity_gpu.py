@@ -326,6 +326,37 @@ def test_host_io_graph_rswa():
     assert dec.device_status() == 0
 
 
+def test_window_end_selection_equals_selecting_warmup():
+    """Ending a profiling window by one focal call on the deepest chosen
+    layer (finish_warmup(q=...) after profile-only steps) gives the same C,
+    the same image mass and the same F_last, bit for bit, as warm-up steps that
+    select in every layer and take F_last from the last of them."""
+    from dynamic_sparse_kv_gb300 import DecodeAttention
+    case = _case("qwen7b_b1", batch=3, layers=5, prompt=24, grid=(1, 12, 16), steps=12,
+                 warmup=4, n_focal=2, tau=0.1)
+    wl = case.wl
+    res = []
+    for select in (True, False):
+        dec = DecodeAttention(case.k_cache, case.v_cache, case.block_table, q_heads=wl.q_heads,
+                              img_range=case.img_range, max_img=wl.n_img, tau=wl.tau)
+        dec.begin_warmup()
+        for t in range(wl.warmup):
+            dec.set_seq_len(wl.seq_len_at(t))
+            q = case.q_at(t).contiguous()
+            dec.warmup_step(q, torch.empty_like(q), select=select)
+        focal, mass = dec.finish_warmup(wl.n_focal, q=None if select else q)
+        idx, k = dec.sel[max(focal)]
+        res.append((focal, mass, idx.cpu(), k.cpu()))
+        assert dec.device_status() == 0
+        dec.close()
+    (f1, m1, i1, k1), (f2, m2, i2, k2) = res
+    assert f1 == f2
+    assert np.allclose(m1, m2, rtol=1e-6, atol=0)   # the two paths sum the mass differently
+    assert torch.equal(k1, k2)
+    for b in range(wl.batch):
+        assert torch.equal(i1[b, :int(k1[b])], i2[b, :int(k2[b])]), b
+
+
 def test_checkpoint_resume():
     """The method's state saved mid-warm-up and again in the steady decode and
     loaded into fresh decoders: the resumed decode gives the same outputs and
