@@ -914,16 +914,18 @@ def test_score_reduce_path_whole_decode():
     assert len(calls) == 2 * (case.wl.steps - case.wl.warmup)   # two focal layers a step
 
 
+@pytest.mark.parametrize("variant", ["auto", "general"])
 @pytest.mark.parametrize("splits", [None, 1, 5])
 @pytest.mark.parametrize("shape", [dict(), dict(q_heads=6, kv_heads=3, head_dim=128, dtype="f32")],
                          ids=["bf16_g7", "f32_g2"])
-def test_profile_attend_mass(shape, splits):
+def test_profile_attend_mass(shape, splits, variant):
     """The profile-only layer (fastocr_profile_attend, the warm-up steps that
     keep no selection): its output is full attention, and the image mass it
     adds to its profiler slot is the oracle's sum over sequences and query
     heads of the image tokens' probabilities, and the mass the focal call
     adds, to within 1e-5 relative; forced split counts merge the mass over a
-    cluster."""
+    cluster, in the automatic variant (deep for these small grids in bf16)
+    and the general one."""
     from dynamic_sparse_kv_gb300 import DecodeAttention
     from dynamic_sparse_kv_gb300 import _native as N
     case = _case("qwen7b_b1", batch=3, layers=2, prompt=37, grid=(1, 24, 20), steps=40, tau=0.1,
@@ -933,7 +935,8 @@ def test_profile_attend_mass(shape, splits):
     n_t = wl.seq_len_at(t)
     dec = DecodeAttention(case.k_cache, case.v_cache, case.block_table, q_heads=wl.q_heads,
                           img_range=case.img_range, max_img=wl.n_img, tau=wl.tau,
-                          splits={0: splits} if splits else None)
+                          splits={0: splits} if splits else None,
+                          variants={0: N.VARIANT_GENERAL} if variant == "general" else None)
     dec.set_seq_len(n_t)
     dec.begin_warmup()                                # profiler slots zeroed
     q = case.q_at(t)[0].contiguous()
